@@ -1,0 +1,220 @@
+"""Model-level pins of the fp64 oracle (CPU only).
+
+Each test checks the oracle against something other than itself: a structural
+property the method fixes (primary flow self-contained, auxiliary flow never
+writes the cache), a special case with a closed form, or an independent
+standard Transformer assembled from torch library routines.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import dfsynth
+from dfsynth.gen import Weights
+from oracle import Oracle
+
+
+def _run(cfg, w, nb=None, steps=None, aux=True, trace=False):
+    nb = nb or cfg.batch
+    tok = dfsynth.tokens(cfg, 0, nb)
+    o = Oracle(cfg, w, nb)
+    o.prefill(tok[:, :cfg.n_prefill])
+    outs = []
+    for s in range(steps or cfg.n_steps):
+        outs.append(o.decode_step(tok[:, cfg.n_prefill + s], aux=aux, trace=trace))
+    return o, outs
+
+
+def _tied(cfg, seed=0, a=0.0, b=0.0, c=0.0):
+    w = Weights(cfg, seed)
+    ov = {("emb2",): w[("emb1",)]}
+    for l in range(cfg.n_layers):
+        ov[(l, "a")] = np.full(cfg.q_dim, a, np.float32)
+        ov[(l, "b")] = np.full(cfg.mlp_hidden, b, np.float32)
+        ov[(l, "c")] = np.full(cfg.d_model, c, np.float32)
+    return Weights(cfg, seed, overrides=ov)
+
+
+CFGS = ["t_fp32", "t_fp32_gqa", "t_bf16", "t_moe"]
+
+
+@pytest.mark.parametrize("name", CFGS)
+def test_primary_self_contained_and_aux_writes_no_cache(name):
+    cfg = dfsynth.get_config(name).with_(n_steps=3)
+    w = Weights(cfg, 0)
+    o_on, on = _run(cfg, w, aux=True)
+    o_off, off = _run(cfg, w, aux=False)
+    for a, b in zip(on, off):
+        np.testing.assert_array_equal(a["logp1"], b["logp1"])
+        np.testing.assert_array_equal(a["topk"], b["topk"])
+    for l in range(cfg.n_layers):
+        for s in range(cfg.batch):
+            np.testing.assert_array_equal(o_on.K[l][s], o_off.K[l][s])
+            np.testing.assert_array_equal(o_on.V[l][s], o_off.V[l][s])
+    # nothing beyond position t was touched
+    assert np.all(o_on.K[0][0][:, o_on.t:] == 0)
+
+
+@pytest.mark.parametrize("name", CFGS)
+def test_zero_coupling_tied_embeddings_collapses_to_primary(name):
+    cfg = dfsynth.get_config(name).with_(n_steps=2)
+    _, outs = _run(cfg, _tied(cfg))
+    for r in outs:
+        np.testing.assert_array_equal(r["logp2"], r["logp1"])
+        np.testing.assert_allclose(r["logp_mix"], r["logp1"], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(r["argmax"], r["argmax1"])
+
+
+@pytest.mark.parametrize("name", CFGS)
+def test_alpha_at_least_half(name):
+    cfg = dfsynth.get_config(name).with_(n_steps=2)
+    _, outs = _run(cfg, Weights(cfg, 0))
+    for r in outs:
+        assert np.all(r["alpha"] >= 0.5) and np.all(r["alpha"] <= 1.0)
+        np.testing.assert_allclose(np.exp(r["logp_mix"]).sum(1), 1.0, atol=1e-12)
+        p1 = np.exp(r["logp1"])
+        np.testing.assert_allclose(r["alpha"], 0.5 + 0.5 * (p1 * p1).sum(1), rtol=1e-14)
+
+
+def test_alpha_spans_range_with_peaked_head():
+    cfg = dfsynth.get_config("t_fp32").with_(n_steps=4, lm_scale=60.0)
+    _, outs = _run(cfg, Weights(cfg, 0))
+    al = np.concatenate([r["alpha"] for r in outs])
+    assert al.min() >= 0.5 and al.max() > 0.6
+
+
+def test_query_coupling_minus_one_gives_uniform_attention():
+    # E2 = E1 and a = -1: in layer 0 the auxiliary pre-RoPE query equals
+    # q1 - q1 = 0, so its attention is the plain average of V[0..t].
+    cfg = dfsynth.get_config("t_fp32_gqa").with_(n_steps=2)
+    o, outs = _run(cfg, _tied(cfg, a=-1.0), trace=True)
+    t = outs[-1]["t"]
+    tr = outs[-1]["trace"][0]
+    assert np.all(tr["Q2"] == 0)
+    G = cfg.group
+    for s in range(cfg.batch):
+        for h in range(cfg.n_heads):
+            mean_v = o.V[0][s][h // G, :t + 1].mean(axis=0)
+            np.testing.assert_allclose(tr["o2"][s].reshape(cfg.n_heads, -1)[h], mean_v, atol=1e-13)
+
+
+@pytest.mark.parametrize("name", ["t_fp32_gqa", "t_moe"])
+@pytest.mark.parametrize("which", ["b", "c"])
+def test_mlp_couplings_minus_one_cancel_layer0_mlp(name, which):
+    # E2 = E1, a = 0: in layer 0 both flows carry the same state.  b = -1
+    # cancels the auxiliary MLP intermediate (z2 = z1 - z1); c = -1 cancels its
+    # MLP output (y2 = y1 - y1).  Either way the layer-0 MLP adds nothing to h2.
+    cfg = dfsynth.get_config(name).with_(n_steps=1)
+    kw = {which: -1.0}
+    _, outs = _run(cfg, _tied(cfg, **kw), trace=True)
+    tr = outs[0]["trace"][0]
+    np.testing.assert_allclose(tr["h2"], tr["h2_attn"], rtol=0, atol=1e-12)
+    # and a layer-0 MLP that is not cancelled does change h2
+    _, outs0 = _run(cfg, _tied(cfg), trace=True)
+    assert np.abs(outs0[0]["trace"][0]["h2"] - outs0[0]["trace"][0]["h2_attn"]).max() > 1e-4
+
+
+def test_moe_single_expert_reduces_to_dense():
+    moe = dfsynth.get_config("t_moe").with_(n_experts=1, top_k=1, n_steps=2)
+    dense = moe.with_(n_experts=0, top_k=0, ffn_hidden=moe.expert_hidden, expert_hidden=0)
+    wm = Weights(moe, 0)
+    ov = {}
+    for l in range(moe.n_layers):
+        for n in ("wg", "wu", "wd"):
+            ov[(l, n)] = wm[(l, 0, n)]
+        ov[(l, "b")] = wm[(l, "b")]
+    wd = Weights(dense, 0, overrides=ov)
+    _, om = _run(moe, wm)
+    _, od = _run(dense, wd)
+    for a, b in zip(om, od):
+        np.testing.assert_allclose(a["logp_mix"], b["logp_mix"], rtol=0, atol=1e-12)
+        assert np.all(a["topk"] == 0)
+
+
+def test_moe_replay_gates_are_normalised_and_shared_set():
+    cfg = dfsynth.get_config("t_moe").with_(n_steps=2)
+    o, outs = _run(cfg, Weights(cfg, 0))
+    for r in outs:
+        k = r["topk"]
+        assert k.shape == (cfg.n_layers, cfg.batch, cfg.top_k)
+        for l in range(cfg.n_layers):
+            for s in range(cfg.batch):
+                assert len(set(k[l, s])) == cfg.top_k
+                # descending router logits
+                rl = r["router1"][l][s][k[l, s]]
+                assert np.all(np.diff(rl) <= 0)
+
+
+@pytest.mark.parametrize("name", CFGS)
+def test_token_serial_decode_equals_prefill(name):
+    # Two code paths of the oracle: the causal-mask prefill over n positions,
+    # and n primary-only steps one position at a time, must write the same KV.
+    cfg = dfsynth.get_config(name)
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    n = 12
+    a = Oracle(cfg, w, cfg.batch)
+    a.prefill(tok[:, :n])
+    b = Oracle(cfg, w, cfg.batch)
+    b.prefill(tok[:, :1])
+    for p in range(1, n):
+        b.decode_step(tok[:, p], aux=False)
+    for l in range(cfg.n_layers):
+        for s in range(cfg.batch):
+            np.testing.assert_allclose(a.K[l][s][:, :n], b.K[l][s][:, :n], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(a.V[l][s][:, :n], b.V[l][s][:, :n], rtol=0, atol=1e-12)
+
+
+def _torch_standard_transformer(cfg, w, tok):
+    """A standard pre-norm causal Transformer over tok[n] from torch library
+    routines (rms_norm, scaled_dot_product_attention, silu, log_softmax); RoPE
+    as a complex rotation of (i, i + hd/2) pairs.  Returns (last-position
+    log-probs, K[l][Hkv][n][hd], V[l])."""
+    T = lambda k: torch.from_numpy(np.asarray(w[k], dtype=np.float64))
+    n = len(tok)
+    hd, Hq, Hkv = cfg.head_dim, cfg.n_heads, cfg.n_kv_heads
+    x = T(("emb1",))[torch.from_numpy(tok.astype(np.int64))]
+    pos = torch.arange(n, dtype=torch.float64)
+    inv = cfg.rope_theta ** (-torch.arange(hd // 2, dtype=torch.float64) * 2 / hd)
+    rot = torch.polar(torch.ones(n, hd // 2, dtype=torch.float64), pos[:, None] * inv[None])
+
+    def rope_c(v):  # v [H][n][hd]
+        z = torch.complex(v[..., : hd // 2], v[..., hd // 2:]) * rot
+        return torch.cat([z.real, z.imag], -1)
+
+    Ks, Vs = [], []
+    for l in range(cfg.n_layers):
+        u = F.rms_norm(x, (cfg.d_model,), weight=T((l, "attn_norm")), eps=cfg.norm_eps)
+        q = (u @ T((l, "wq")).T).view(n, Hq, hd).transpose(0, 1)
+        k = (u @ T((l, "wk")).T).view(n, Hkv, hd).transpose(0, 1)
+        v = (u @ T((l, "wv")).T).view(n, Hkv, hd).transpose(0, 1)
+        q, k = rope_c(q), rope_c(k)
+        Ks.append(k.numpy())
+        Vs.append(v.numpy())
+        o = F.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, enable_gqa=True)[0]
+        x = x + o.transpose(0, 1).reshape(n, -1) @ T((l, "wo")).T
+        u = F.rms_norm(x, (cfg.d_model,), weight=T((l, "mlp_norm")), eps=cfg.norm_eps)
+        x = x + (F.silu(u @ T((l, "wg")).T) * (u @ T((l, "wu")).T)) @ T((l, "wd")).T
+    u = F.rms_norm(x, (cfg.d_model,), weight=T(("final_norm",)), eps=cfg.norm_eps)
+    return torch.log_softmax(u[-1] @ T(("lm_head",)).T, -1).numpy(), Ks, Vs
+
+
+@pytest.mark.parametrize("name", ["t_fp32", "t_fp32_gqa"])
+def test_primary_flow_is_a_standard_transformer(name):
+    cfg = dfsynth.get_config(name)
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    P = cfg.n_prefill + 1
+    o = Oracle(cfg, w, cfg.batch)
+    o.prefill(tok[:, :P - 1])
+    r = o.decode_step(tok[:, P - 1], aux=True)
+    for s in range(cfg.batch):
+        lp, Ks, Vs = _torch_standard_transformer(cfg, w, tok[s, :P])
+        np.testing.assert_allclose(r["logp1"][s], lp, rtol=0, atol=1e-11)
+        for l in range(cfg.n_layers):
+            np.testing.assert_allclose(o.K[l][s][:, :P], Ks[l], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(o.V[l][s][:, :P], Vs[l], rtol=0, atol=1e-12)
