@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Decode throughput of the grouped dual-flow step on B300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one df_decode_step: both flows of B sequences at one position
+(embedding, every layer, LM head, mixture), teacher-forced from the seed.
+The default workload is the dense ~1B model at batch 16 with the cache
+prefilled to 1023 positions.  With N > 1 (torchrun, one process per GPU)
+every rank runs an independent replica of the workload: the path shards over
+sequences with no exchange, so the value is the aggregate over ranks and the
+scaling is weak.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dual-flow decode tokens/s @1xB300; achieved HBM GB/s vs roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j.get("bf16_tflops", 1816.0)), "measured"
+    except Exception:
+        return 6400.0, 1800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if sm:
+            out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                   "samples": len(sm)}
+        return out
+
+
+def algorithmic_bytes(cfg, op: str, B: int, t: int, moe_union: float | None = None) -> float:
+    """Bytes one launch of an operation must move: weights read once, KV read
+    once, KV appended, logits written."""
+    esz = 2 if cfg.dtype == "bf16" else 4
+    d, qd, kvd, F = cfg.d_model, cfg.q_dim, cfg.kv_dim, cfg.ffn_hidden
+    if op == "qkv":
+        return (qd + 2 * kvd) * d * esz + 2 * B * kvd * esz
+    if op == "attn":
+        return 2.0 * B * kvd * (t + 1) * esz
+    if op == "wo":
+        return d * qd * esz
+    if op == "gateup":
+        return 2 * F * d * esz
+    if op == "down":
+        return d * F * esz
+    if op == "lmhead":
+        return cfg.vocab * d * esz + 2 * B * cfg.vocab * 4
+    if op == "moe":
+        touched = moe_union if moe_union is not None else cfg.n_experts
+        return cfg.n_experts * d * esz + touched * 3 * cfg.expert_hidden * d * esz
+    raise KeyError(op)
+
+
+def step_bytes(cfg, B: int, t: int, moe_union: float | None = None) -> float:
+    L = cfg.n_layers
+    per_layer = algorithmic_bytes(cfg, "qkv", B, t) + algorithmic_bytes(cfg, "attn", B, t) + \
+        algorithmic_bytes(cfg, "wo", B, t)
+    if cfg.n_experts:
+        per_layer += algorithmic_bytes(cfg, "moe", B, t, moe_union)
+    else:
+        per_layer += algorithmic_bytes(cfg, "gateup", B, t) + algorithmic_bytes(cfg, "down", B, t)
+    esz = 2 if cfg.dtype == "bf16" else 4
+    return L * per_layer + cfg.vocab * cfg.d_model * esz + 2 * B * cfg.d_model * esz + B * cfg.vocab * 4
+
+
+# ------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import dfsynth
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    cfg = dfsynth.get_config(args.config)
+    B, P = cfg.batch, cfg.n_prefill
+    K, W = args.steps, args.warmup
+    span = max(cfg.n_steps, W + K)
+    max_len = P + span
+    tok = dfsynth.tokens(cfg.with_(n_steps=span), args.seed + rank)
+    model = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, args.seed, dev), max_batch=B, max_len=max_len,
+                          device=dev)
+    tok_d = torch.from_numpy(tok).to(dev)
+    model.prefill(tok_d[:, :P].contiguous())
+    model.sync()
+    steps_tok = tok_d[:, P:].t().contiguous()          # [span][B]
+    lp = torch.empty(B, cfg.vocab, device=dev)
+    am = torch.empty(B, dtype=torch.int32, device=dev)
+    al = torch.empty(B, device=dev)
+    stream = model.stream
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def timed(n_warm, n_timed):
+        for s in range(n_warm):
+            model.decode_step(steps_tok[s], lp, am, al)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(n_warm, n_warm + n_timed):
+            model.decode_step(steps_tok[s], lp, am, al)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return e0.elapsed_time(e1)
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # main measurement: grouped step
+    clocks = Clocks(local_rank)
+    clocks.start()
+    ms_total = timed(W, K)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(ms_total)
+    kernels = model.step_kernels
+    ms_step = ms_total / K
+    tokens_s = world * B * K / (ms_total / 1e3)
+    t_mid = P + W + K // 2
+
+    # ablations on the same positions: two ungrouped passes, and primary-only decode
+    abl = {}
+    for name, aux, ung in (("ungrouped_two_pass", 1, 1), ("aux_off_standard_decode", 0, 0)):
+        model.set_length(B, P)
+        model.set_mode(aux, ung)
+        kk = min(K, 32)
+        ms = max_over_ranks(timed(min(W, 3), kk)) / kk
+        abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1)}
+    model.set_mode(1, 0)
+
+    # dominant operation: time every op, cycling layers, with CUDA events
+    model.set_length(B, t_mid)
+    model.decode_step(steps_tok[0], lp, am, al)
+    ops = ["qkv", "attn", "wo"] + (["moe"] if cfg.n_experts else ["gateup", "down"]) + ["lmhead"]
+    per_step_count = {o: (1 if o == "lmhead" else cfg.n_layers) for o in ops}
+    op_ms = {}
+    for o in ops:
+        model.time_op(o, 2)
+        op_ms[o] = model.time_op(o, max(4, 2 * cfg.n_layers) if o != "lmhead" else 8)
+    shares = {o: op_ms[o] * per_step_count[o] for o in ops}
+    dom = max(shares, key=shares.get)
+    hbm_peak, _, peak_kind = _peaks()
+    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mid + 1)
+    achieved = bytes_dom / (op_ms[dom] / 1e3) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "peak_source": peak_kind, "ms_per_launch": round(op_ms[dom], 5),
+                "algorithmic_bytes_per_launch": bytes_dom}
+    sb = step_bytes(cfg, B, t_mid)
+    step_gbs = sb / (ms_step / 1e3) / 1e9
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    model.set_length(B, P)
+    h_tok = torch.from_numpy(tok[:, P:].T.copy()).pin_memory()
+    h_lp = torch.empty(B, cfg.vocab).pin_memory()
+    h_am = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_al = torch.empty(B).pin_memory()
+    for s in range(min(W, 3)):
+        model.decode_step_host(h_tok[s], h_lp, h_am, h_al)
+    barrier()
+    t0 = time.perf_counter()
+    ke = min(K, span - min(W, 3))
+    for s in range(min(W, 3), min(W, 3) + ke):
+        model.decode_step_host(h_tok[s], h_lp, h_am, h_al)
+    t1 = time.perf_counter()
+    barrier()
+    e2e_s = max_over_ranks(t1 - t0)
+    e2e = {"value": round(world * B * ke / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": B * 4,
+           "d2h_bytes_per_step": B * cfg.vocab * 4 + B * 4 + B * 4}
+
+    result = {
+        "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": B, "stacked_rows": 2 * B, "context_at_first_step": P,
+                   "layers": cfg.n_layers, "d_model": cfg.d_model, "vocab": cfg.vocab,
+                   "experts": cfg.n_experts, "l2": "inputs larger than L2 (weights + KV per step >> 126 MB)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+        "step_hbm": {"algorithmic_bytes": sb, "achieved_gbs": round(step_gbs, 1),
+                     "frac_of_measured": round(step_gbs / hbm_peak, 4), "frac_of_8tbs": round(step_gbs / 8000, 4)},
+        "roofline": roofline,
+        "ops_ms_per_launch": {o: round(v, 5) for o, v in op_ms.items()},
+        "ablation": abl,
+        "e2e": e2e,
+        "gpu_launches": kernels * K if kernels >= 0 else None,
+        "kernels_per_step": kernels,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=args.cpu_budget)
+    model.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------------------------- oracle (CPU) arm
+
+def _oracle_sample(cfg, seed, n_layers, extra=8):
+    """Oracle for one sequence of the workload, with the cache filled to the
+    workload's context from the seeded synthetic-cache generator."""
+    import numpy as np
+    import dfsynth
+    from dfsynth.gen import Weights, synthetic_kv_block
+    from oracle import Oracle
+    sub = cfg.with_(n_layers=n_layers)
+    w = Weights(sub, seed, max_cached=None if not sub.n_experts else 4 * sub.top_k * 3 * sub.n_layers)
+    if not sub.n_experts:
+        w.prefetch()
+    o = Oracle(sub, w, 1, max_len=cfg.n_prefill + extra)
+    for l in range(n_layers):
+        K, V = synthetic_kv_block(sub, seed, l, 0, cfg.n_prefill)
+        o.set_cache(0, l, K, V)
+    o.set_length(cfg.n_prefill)
+    toks = dfsynth.tokens(cfg, seed, batch=1)[0, cfg.n_prefill:]
+    return o, toks
+
+
+def cpu_baseline(cfg, seed, budget_s=30.0):
+    """Oracle decode of one sequence on the host cores, scaled to tokens/s."""
+    import numpy as np
+    cores = len(os.sched_getaffinity(0))
+    n_l = cfg.n_layers
+    # size the sample: estimate one layer first
+    o, toks = _oracle_sample(cfg, seed, 1)
+    o.decode_step(toks[:1])
+    t0 = time.perf_counter()
+    o.decode_step(toks[1:2])
+    per_layer = time.perf_counter() - t0
+    n_l = max(1, min(cfg.n_layers, int(budget_s / max(per_layer, 1e-3) / 2)))
+    o, toks = _oracle_sample(cfg, seed, n_l)
+    o.decode_step(toks[:1])
+    t0 = time.perf_counter()
+    o.decode_step(toks[1:2])
+    dt = time.perf_counter() - t0
+    est_step = dt * cfg.n_layers / n_l
+    return {"value": round(1.0 / est_step, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one sequence of {cfg.batch}, one decode step at position {cfg.n_prefill + 1}, "
+                      f"{n_l} of {cfg.n_layers} layers (time scaled by layer count), synthetic cache"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import dfsynth
+    cfg = dfsynth.get_config(args.config)
+    cores = len(os.sched_getaffinity(0))
+    K, W = args.steps, args.warmup
+    # per-step sample: one sequence through n_l layers, sized to keep the run to a few minutes
+    o, toks = _oracle_sample(cfg, args.seed, 1)
+    o.decode_step(toks[:1])
+    t0 = time.perf_counter()
+    o.decode_step(toks[1:2])
+    per_layer = time.perf_counter() - t0
+    n_l = max(1, min(cfg.n_layers, int(120.0 / max(per_layer * (K + W), 1e-3))))
+    o, toks = _oracle_sample(cfg, args.seed, n_l, extra=K + W + 2)
+    toks_all = dfsynth.tokens(cfg.with_(n_steps=K + W + 2), args.seed, batch=1)[0, cfg.n_prefill:]
+    for s in range(W):
+        o.decode_step(toks_all[s:s + 1])
+    t0 = time.perf_counter()
+    for s in range(W, W + K):
+        o.decode_step(toks_all[s:s + 1])
+    dt = (time.perf_counter() - t0) / K * cfg.n_layers / n_l
+    value = 1.0 / dt
+    sample = (f"each step: one sequence of {cfg.batch}, one decode position, {n_l} of {cfg.n_layers} layers "
+              f"(time scaled by layer count), synthetic cache at context {cfg.n_prefill}")
+    return {"metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "context_at_first_step": cfg.n_prefill},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--config", default="dense1b_ctx1k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

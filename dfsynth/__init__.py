@@ -10,6 +10,7 @@ mixes or routes.
 from .configs import DFConfig, WORKLOADS, TEST_CONFIGS, get_config  # noqa: F401
 from .gen import (  # noqa: F401
     Weights,
+    DeviceWeights,
     tokens,
     synthetic_kv_block,
     bf16_round_f32,

@@ -185,3 +185,33 @@ def synthetic_kv_block(cfg, seed: int, layer: int, b: int, n_pos: int, std: floa
         z = g.standard_normal(size=(cfg.n_kv_heads, n_pos, cfg.head_dim), dtype=np.float32)
         out.append(bf16_round_f32(z * np.float32(std)) if cfg.dtype == "bf16" else z * np.float32(std))
     return out[0], out[1]
+
+
+class DeviceWeights:
+    """Weights of the same shapes and distributions drawn on a CUDA device
+    with torch's generator (fast set-up for timing runs; the values differ
+    from ``Weights``, so these are never compared with the oracle)."""
+
+    def __init__(self, cfg, seed: int = 0, device="cuda"):
+        self.cfg = cfg
+        self.seed = seed
+        self.device = device
+
+    def __getitem__(self, key: tuple):
+        import torch
+        shape = tensor_shape(self.cfg, key)
+        g = torch.Generator(device=self.device)
+        g.manual_seed(self.seed * 1_000_003 + tensor_id(key))
+        z = torch.randn(shape, generator=g, device=self.device, dtype=torch.float32)
+        kind = _kind(key)
+        if kind == "gain":
+            return 1.0 + self.cfg.gain_std * z
+        if kind == "coupling":
+            return self.cfg.coup_std * z
+        std = self.cfg.router_sigma if kind == "router" else self.cfg.w_std
+        if key == ("lm_head",):
+            std = std * self.cfg.lm_scale
+        return (z * std).to(torch.bfloat16).to(torch.float32)
+
+    def keys(self) -> list:
+        return all_keys(self.cfg)

@@ -1,0 +1,121 @@
+// Internal interface between the C-ABI runtime (df_runtime.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace df {
+
+// Model dimensions plus derived sizes, fixed at df_create.
+struct Dims {
+  int L, d, Hq, Hkv, hd, F, V, E, k, Fe;
+  float theta, eps;
+  int bf16;        // 1: bf16 storage, 0: fp32
+  int maxB, max_len;
+  int qdim, kvdim, qkvn, G, Fm;   // Fm = MLP hidden of one expert or of the dense MLP
+  int esz;         // element size of dtype
+};
+
+// Device buffers carved out of the caller's workspace.
+struct Buffers {
+  Ctrl* ctrl;
+  int* tokbuf;      // [maxB]   tokens of a host-buffer step
+  float* h;         // [2maxB][d] fp32 residual rows (0..B-1 primary, B..2B-1 auxiliary)
+  void* u;          // [Mpad][d]  normed rows (GEMM input, dtype)
+  float* un;        // [2maxB][d] normed rows, unrounded (router input)
+  float* qatt;      // [2maxB][qdim] rotated, quantised queries
+  void* o;          // [Mpad][qdim] attention output (GEMM input, dtype)
+  void* z;          // [Mpad][F]  SwiGLU output (GEMM input, dtype)
+  float* raw;       // [Mpad][rawN] fp32 GEMM output before the epilogue (CUDA-core path)
+  int rawN;
+  float* logits;    // [2maxB][V]
+  float* part_o;    // attention split partials: [parts][hd]
+  float* part_ml;   // [parts][2] (running max, running sum)
+  size_t parts_cap; // number of (b, kv head, split, row) partial slots
+  float* q1s;       // [L][maxB][qdim] saved primary pre-RoPE queries (ungrouped)
+  float* z1s;       // [L][maxB][F] (MoE: [L][maxB][k][Fe]) saved primary MLP hidden
+  float* y1s;       // [L][maxB][d] saved primary MLP output
+  float* rlog;      // [2maxB][E] router logits
+  int* topk;        // [L][maxB][k] primary expert sets
+  float* gate;      // [2maxB][k] gate weights per row
+  int* ecount;      // [E]
+  int* elist;       // [E][maxB] entries b*k + j
+  void* zE;         // [2][maxB][k][Fe] expert hidden (dtype)
+  float* yE;        // [2][maxB][k][d] expert outputs fp32
+  float* out_logp;  // [maxB][V] host-step staging
+  int* out_arg;     // [maxB]
+  float* out_alpha; // [maxB]
+  float* rope;      // [max_len][hd/2][2] cos, sin
+  int* tickets;     // split-K tile tickets
+  size_t tickets_cap;
+  float* gpart;     // split-K partial tiles
+  size_t gpart_cap; // floats
+};
+
+// Which rows of the stacked block a launch works on.
+struct Rows {
+  int B;        // batch
+  int lo, hi;   // active stacked rows [lo, hi): [0,B) primary, [B,2B) auxiliary, [0,2B) both
+  bool has_primary() const { return lo < B; }
+  bool has_aux() const { return hi > B; }
+};
+
+// Coupling sources for the auxiliary rows of one layer.
+//  grouped   (saved == 0): the primary values come from the same launch (rows 0..B-1)
+//  ungrouped (saved == 1): they come from the q1s / z1s / y1s buffers of layer l
+struct Couple {
+  int saved;    // read partners from the saved buffers
+  int save;     // write primary values to the saved buffers
+  float* q1s;   // layer slice
+  float* z1s;
+  float* y1s;
+};
+
+// ------------------------------------------------------------ basic kernels
+void kernels_init();   // one-time function attributes (dynamic shared memory limits)
+void launch_set_pos(Ctrl* c, int t, cudaStream_t s);
+void launch_advance_pos(Ctrl* c, cudaStream_t s);
+void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void* emb2,
+                  const int32_t* tokens, int tok_stride, int use_pos, const Rows& R, cudaStream_t s);
+void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out, float* out_f32,
+                    const Rows& R, cudaStream_t s);
+
+// CUDA-core GEMV: out[m][n] = sum_k W[n][k] X[m][k] for rows m in [lo, hi).
+// x_f32: X is fp32 (router) instead of dtype.
+void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, int x_f32,
+                 float* out, int ldo, const Rows& R, cudaStream_t s);
+
+// Epilogues over the fp32 GEMM output `raw`.
+void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* a,
+                   void* kv, int layer, const Couple& C, const Rows& R, cudaStream_t s);
+void launch_ep_swiglu(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* bvec,
+                      const Couple& C, const Rows& R, cudaStream_t s);
+void launch_ep_down(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* cvec,
+                    const Couple& C, const Rows& R, cudaStream_t s);
+void launch_ep_residual(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const Rows& R,
+                        cudaStream_t s);
+
+// Attention (split-KV) and the merge of split partials into o.
+int attn_splits(const Dims& D, int B);
+void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, int layer, int splits,
+                              const Rows& R, cudaStream_t s);
+void launch_attn_combine(const Dims& D, const Buffers& Bf, int splits, const Rows& R, cudaStream_t s);
+
+// Softmax / mixture / argmax.
+void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax,
+                float* alpha, float* logp1, float* logp2, cudaStream_t s);
+
+// MoE with router replay.
+void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R,
+                      int32_t* dbg_topk, float* dbg_router, cudaStream_t s);
+void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu, const float* bvec,
+                               const Couple& C, const Rows& R, cudaStream_t s);
+void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, const Rows& R,
+                             cudaStream_t s);
+void launch_moe_combine(const Dims& D, const Buffers& Bf, const float* cvec, const Couple& C,
+                        const Rows& R, cudaStream_t s);
+
+}  // namespace df

@@ -1,0 +1,696 @@
+// C-ABI runtime of the dual-flow decode library: configuration checks,
+// workspace layout, the per-step kernel sequence, CUDA-graph capture and
+// replay, and device error reporting.
+//
+// Step sequence ("Arquitectura Central" and "Mecanismos Clave" of "Resumen
+// Técnico: Dual-Flow Transformers"):
+//   prefill position:  embed(primary) -> per layer [norm, QKV+RoPE+append,
+//                      attention, Wo+residual, norm, MLP] -> advance t
+//   grouped decode:    embed(both flows, stacked) -> per layer the same chain
+//                      over 2B rows with the a/b/c couplings in the epilogues
+//                      -> final norm -> LM head -> mixture -> advance t
+//   ungrouped decode:  the same layers run once for the primary rows (saving
+//                      q1, z1, y1) and once more for the auxiliary rows.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "df.h"
+#include "df_internal.h"
+#include "tc_gemm.h"
+#include "attn_fast.h"
+
+using df::Buffers;
+using df::Couple;
+using df::Dims;
+using df::Rows;
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct GraphKey {
+  const void* p[8];
+  int i[6];
+  bool operator==(const GraphKey& o) const {
+    return memcmp(p, o.p, sizeof(p)) == 0 && memcmp(i, o.i, sizeof(i)) == 0;
+  }
+};
+
+struct GraphSlot {
+  bool valid = false;
+  GraphKey key{};
+  cudaGraphExec_t exec = nullptr;
+  int kernels = 0;
+  void reset() {
+    if (exec) cudaGraphExecDestroy(exec);
+    exec = nullptr;
+    valid = false;
+  }
+};
+
+}  // namespace
+
+struct df_ctx {
+  df_config cfg{};
+  Dims D{};
+  Buffers Bf{};
+  const void *emb1 = nullptr, *emb2 = nullptr, *lm_head = nullptr;
+  const float* final_norm = nullptr;
+  std::vector<const float*> attn_norm, mlp_norm, a, b, c;
+  std::vector<const void*> wqkv, wo, wgu, wd, router;
+  void* kv = nullptr;
+  char* ws = nullptr;
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  int B = 0, t = 0, splits = 1;
+  bool ready = false;
+  int aux_on = 1, ungrouped = 0;
+  float *dbg_logp1 = nullptr, *dbg_logp2 = nullptr, *dbg_router = nullptr;
+  int32_t* dbg_topk = nullptr;
+  bool use_graph = true;
+  int force_generic = 0;
+  GraphSlot dec, pre;
+  int last_kernels = -1;
+  df::TcPlan tc;
+  df::AttnPlan at;
+  std::string err;
+};
+
+namespace {
+
+df_status fail(df_ctx* X, df_status st, const std::string& msg) {
+  if (X) X->err = msg;
+  return st;
+}
+
+df_status cuda_fail(df_ctx* X, cudaError_t e, const char* where) {
+  return fail(X, DF_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+bool valid_config(const df_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (!c) return bad("null config");
+  if (c->n_layers <= 0 || c->d_model <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->vocab <= 0)
+    return bad("non-positive model size");
+  if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+  if (c->head_dim % 2) return bad("head_dim must be even (RoPE pairs)");
+  if (c->dtype != DF_F32 && c->dtype != DF_BF16) return bad("dtype must be DF_F32 or DF_BF16");
+  if (c->max_batch <= 0 || c->max_len <= 0) return bad("max_batch and max_len must be positive");
+  if (c->max_batch > 4096) return bad("max_batch above 4096");
+  if (c->n_experts < 0) return bad("n_experts < 0");
+  if (c->n_experts == 0) {
+    if (c->ffn_hidden <= 0 || c->ffn_hidden % 64) return bad("ffn_hidden must be a positive multiple of 64");
+  } else {
+    if (c->top_k <= 0 || c->top_k > c->n_experts || c->top_k > 16) return bad("top_k must be in [1, min(16, E)]");
+    if (c->expert_hidden <= 0 || c->expert_hidden % 64) return bad("expert_hidden must be a positive multiple of 64");
+  }
+  if (!(c->norm_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("norm_eps and rope_theta must be positive");
+  return true;
+}
+
+Dims make_dims(const df_config* c) {
+  Dims D{};
+  D.L = c->n_layers;
+  D.d = c->d_model;
+  D.Hq = c->n_heads;
+  D.Hkv = c->n_kv_heads;
+  D.hd = c->head_dim;
+  D.F = c->n_experts ? 0 : c->ffn_hidden;
+  D.V = c->vocab;
+  D.E = c->n_experts;
+  D.k = c->n_experts ? c->top_k : 0;
+  D.Fe = c->n_experts ? c->expert_hidden : 0;
+  D.theta = c->rope_theta;
+  D.eps = c->norm_eps;
+  D.bf16 = c->dtype == DF_BF16;
+  D.maxB = c->max_batch;
+  D.max_len = c->max_len;
+  D.qdim = D.Hq * D.hd;
+  D.kvdim = D.Hkv * D.hd;
+  D.qkvn = D.qdim + 2 * D.kvdim;
+  D.G = D.Hq / D.Hkv;
+  D.Fm = D.E ? D.Fe : D.F;
+  D.esz = D.bf16 ? 2 : 4;
+  return D;
+}
+
+// Carves the workspace.  With base == nullptr only the size is computed.
+size_t layout(const Dims& D, Buffers* Bf, char* base) {
+  size_t cur = 0;
+  auto take = [&](size_t bytes) -> char* {
+    size_t o = cur;
+    cur = align_up(cur + (bytes ? bytes : 1), 256);
+    return base ? base + o : nullptr;
+  };
+  size_t M2 = 2 * (size_t)D.maxB, Mpad = align_up(M2, 16);
+  size_t esz = D.esz;
+  Buffers b{};
+  b.ctrl = (df::Ctrl*)take(sizeof(df::Ctrl));
+  b.tokbuf = (int*)take(D.maxB * 4);
+  b.h = (float*)take(M2 * D.d * 4);
+  b.u = take(Mpad * D.d * esz);
+  b.un = (float*)take(D.E ? M2 * D.d * 4 : 0);
+  b.qatt = (float*)take(M2 * D.qdim * 4);
+  b.o = take(Mpad * D.qdim * esz);
+  b.z = take(Mpad * (size_t)D.F * esz);
+  size_t rawN = D.qkvn;
+  if ((size_t)2 * D.F > rawN) rawN = 2 * D.F;
+  if ((size_t)D.d > rawN) rawN = D.d;
+  if ((size_t)D.E > rawN) rawN = D.E;
+  b.rawN = (int)rawN;
+  b.raw = (float*)take(Mpad * rawN * 4);
+  b.logits = (float*)take(M2 * D.V * 4);
+  size_t parts = 0;
+  for (int B = 1; B <= D.maxB; ++B) {
+    size_t p = (size_t)B * D.Hkv * df::attn_splits(D, B) * 2 * D.G;
+    if (p > parts) parts = p;
+  }
+  b.parts_cap = parts;
+  b.part_o = (float*)take(parts * D.hd * 4);
+  b.part_ml = (float*)take(parts * 2 * 4);
+  size_t zs = D.E ? (size_t)D.k * D.Fe : (size_t)D.F;
+  b.q1s = (float*)take((size_t)D.L * D.maxB * D.qdim * 4);
+  b.z1s = (float*)take((size_t)D.L * D.maxB * zs * 4);
+  b.y1s = (float*)take((size_t)D.L * D.maxB * D.d * 4);
+  b.rlog = (float*)take(D.E ? M2 * D.E * 4 : 0);
+  b.topk = (int*)take(D.E ? (size_t)D.L * D.maxB * D.k * 4 : 0);
+  b.gate = (float*)take(D.E ? M2 * D.k * 4 : 0);
+  b.ecount = (int*)take(D.E * 4);
+  b.elist = (int*)take((size_t)D.E * D.maxB * 4);
+  b.zE = take(D.E ? 2 * (size_t)D.maxB * D.k * D.Fe * esz : 0);
+  b.yE = (float*)take(D.E ? 2 * (size_t)D.maxB * D.k * D.d * 4 : 0);
+  b.out_logp = (float*)take((size_t)D.maxB * D.V * 4);
+  b.out_arg = (int*)take(D.maxB * 4);
+  b.out_alpha = (float*)take(D.maxB * 4);
+  b.rope = (float*)take((size_t)D.max_len * D.hd * 4);
+  b.tickets_cap = df::tc_tickets_needed(D);
+  b.tickets = (int*)take(b.tickets_cap * 4);
+  b.gpart_cap = df::tc_partial_floats(D);
+  b.gpart = (float*)take(b.gpart_cap * 4);
+  if (Bf) *Bf = b;
+  return cur;
+}
+
+size_t kv_size(const Dims& D) {
+  return (size_t)D.L * 2 * D.maxB * D.Hkv * D.max_len * D.hd * D.esz;
+}
+
+// ---------------------------------------------------------------- step sequencing
+
+struct StepOut {
+  float* logp_mix;
+  int32_t* argmax;
+  float* alpha;
+};
+
+Couple layer_couple(df_ctx* X, int l, int save, int saved) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  size_t zs = D.E ? (size_t)D.k * D.Fe : (size_t)D.F;
+  return Couple{saved, save, Bf.q1s + (size_t)l * D.maxB * D.qdim, Bf.z1s + (size_t)l * D.maxB * zs,
+                Bf.y1s + (size_t)l * D.maxB * D.d};
+}
+
+// QKV projection + Q2 coupling + RoPE + cache append (input: normed rows u).
+void op_qkv(df_ctx* X, int l, const Rows& R, const Couple& C) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::QKV)) {
+    df::tc_qkv(X->tc, D, Bf, X->wqkv[l], X->a[l], X->kv, l, C, R, X->stream);
+  } else {
+    df::launch_gemv(D, X->wqkv[l], D.qkvn, D.d, Bf.u, D.d, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_ep_qkv(D, Bf, Bf.raw, Bf.rawN, X->a[l], X->kv, l, C, R, X->stream);
+  }
+}
+
+// Shared-KV attention of the active query rows, then the split merge.
+void op_attn(df_ctx* X, int l, const Rows& R) {
+  const Dims& D = X->D;
+  if (!X->force_generic && df::attn_fast_can_run(X->at, D)) {
+    df::attn_fast(X->at, D, X->Bf, X->kv, l, X->splits, R, X->stream);
+  } else {
+    df::launch_attention_generic(D, X->Bf, X->kv, l, X->splits, R, X->stream);
+  }
+  df::launch_attn_combine(D, X->Bf, X->splits, R, X->stream);
+}
+
+// Output projection + residual.
+void op_wo(df_ctx* X, int l, const Rows& R) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::RESID)) {
+    df::tc_resid(X->tc, D, Bf, X->wo[l], R, X->stream);
+  } else {
+    df::launch_gemv(D, X->wo[l], D.d, D.qdim, Bf.o, D.qdim, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_ep_residual(D, Bf, Bf.raw, Bf.rawN, R, X->stream);
+  }
+}
+
+// Dense MLP, first half: gate/up + SwiGLU + b coupling.
+void op_gateup(df_ctx* X, int l, const Rows& R, const Couple& C) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::SWIGLU)) {
+    df::tc_swiglu(X->tc, D, Bf, X->wgu[l], X->b[l], C, R, X->stream);
+  } else {
+    df::launch_gemv(D, X->wgu[l], 2 * D.F, D.d, Bf.u, D.d, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_ep_swiglu(D, Bf, Bf.raw, Bf.rawN, X->b[l], C, R, X->stream);
+  }
+}
+
+// Dense MLP, second half: down + c coupling + residual.
+void op_down(df_ctx* X, int l, const Rows& R, const Couple& C) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::DOWN)) {
+    df::tc_down(X->tc, D, Bf, X->wd[l], X->c[l], C, R, X->stream);
+  } else {
+    df::launch_gemv(D, X->wd[l], D.d, D.F, Bf.z, D.F, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_ep_down(D, Bf, Bf.raw, Bf.rawN, X->c[l], C, R, X->stream);
+  }
+}
+
+// MoE MLP with router replay (input: normed rows u and unrounded un).
+void op_moe(df_ctx* X, int l, const Rows& R, const Couple& C) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  cudaStream_t s = X->stream;
+  df::launch_gemv(D, X->router[l], D.E, D.d, Bf.un, D.d, 1, Bf.rlog, D.E, R, s);
+  df::launch_moe_route(D, Bf, l, R.has_primary() ? 1 : 0, R, X->dbg_topk, X->dbg_router, s);
+  df::launch_moe_gateup_generic(D, Bf, X->wgu[l], X->b[l], C, R, s);
+  df::launch_moe_down_generic(D, Bf, X->wd[l], R, s);
+  df::launch_moe_combine(D, Bf, X->c[l], C, R, s);
+}
+
+// LM head over the final-normed rows.
+void op_lm(df_ctx* X, const Rows& R) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::LOGITS)) {
+    df::tc_logits(X->tc, D, Bf, X->lm_head, R, X->stream);
+  } else {
+    df::launch_gemv(D, X->lm_head, D.V, D.d, Bf.u, D.d, 0, Bf.logits, D.V, R, X->stream);
+  }
+}
+
+void enqueue_pass(df_ctx* X, const Rows& R, int save, int saved, bool lm) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  cudaStream_t s = X->stream;
+  for (int l = 0; l < D.L; ++l) {
+    Couple C = layer_couple(X, l, save, saved);
+    df::launch_rmsnorm(D, Bf, X->attn_norm[l], Bf.u, nullptr, R, s);
+    op_qkv(X, l, R, C);
+    op_attn(X, l, R);
+    op_wo(X, l, R);
+    df::launch_rmsnorm(D, Bf, X->mlp_norm[l], Bf.u, D.E ? Bf.un : nullptr, R, s);
+    if (D.E) {
+      op_moe(X, l, R, C);
+    } else {
+      op_gateup(X, l, R, C);
+      op_down(X, l, R, C);
+    }
+  }
+  if (lm) {
+    df::launch_rmsnorm(D, Bf, X->final_norm, Bf.u, nullptr, R, s);
+    op_lm(X, R);
+  }
+}
+
+void enqueue_decode(df_ctx* X, const int32_t* tokens, const StepOut& o) {
+  const Dims& D = X->D;
+  int B = X->B;
+  cudaStream_t s = X->stream;
+  Rows both{B, 0, X->aux_on ? 2 * B : B};
+  df::launch_embed(D, X->Bf, X->emb1, X->emb2, tokens, 1, 0, both, s);
+  if (X->aux_on && X->ungrouped) {
+    enqueue_pass(X, Rows{B, 0, B}, 1, 0, true);
+    enqueue_pass(X, Rows{B, B, 2 * B}, 0, 1, true);
+  } else {
+    enqueue_pass(X, both, 0, 0, true);
+  }
+  df::launch_mix(D, X->Bf, B, X->aux_on, o.logp_mix, o.argmax, o.alpha, X->dbg_logp1, X->aux_on ? X->dbg_logp2 : nullptr,
+                 s);
+  df::launch_advance_pos(X->Bf.ctrl, s);
+}
+
+void enqueue_prefill_pos(df_ctx* X, const int32_t* tokens, int n) {
+  Rows R{X->B, 0, X->B};
+  df::launch_embed(X->D, X->Bf, X->emb1, X->emb2, tokens, n, 1, R, X->stream);
+  enqueue_pass(X, R, 0, 0, false);
+  df::launch_advance_pos(X->Bf.ctrl, X->stream);
+}
+
+int count_kernel_nodes(cudaGraph_t g) {
+  size_t n = 0;
+  if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess) return -1;
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return -1;
+  int k = 0;
+  for (auto& nd : nodes) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++k;
+  }
+  return k;
+}
+
+template <typename F>
+df_status run_captured(df_ctx* X, GraphSlot& slot, const GraphKey& key, F&& enqueue, int repeat) {
+  if (!X->use_graph) {
+    for (int r = 0; r < repeat; ++r) enqueue();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(X, e, "kernel launch");
+    X->last_kernels = -1;
+    return DF_OK;
+  }
+  if (!slot.valid || !(slot.key == key)) {
+    slot.reset();
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(X->stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(X, e, "cudaStreamBeginCapture");
+    enqueue();
+    cudaError_t le = cudaGetLastError();
+    e = cudaStreamEndCapture(X->stream, &g);
+    if (le != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return cuda_fail(X, le, "kernel launch during capture");
+    }
+    if (e != cudaSuccess) return cuda_fail(X, e, "cudaStreamEndCapture");
+    slot.kernels = count_kernel_nodes(g);
+    e = cudaGraphInstantiate(&slot.exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) {
+      slot.exec = nullptr;
+      return cuda_fail(X, e, "cudaGraphInstantiate");
+    }
+    slot.key = key;
+    slot.valid = true;
+  }
+  for (int r = 0; r < repeat; ++r) {
+    cudaError_t e = cudaGraphLaunch(slot.exec, X->stream);
+    if (e != cudaSuccess) return cuda_fail(X, e, "cudaGraphLaunch");
+  }
+  X->last_kernels = slot.kernels;
+  return DF_OK;
+}
+
+void setup_rope(df_ctx* X, std::vector<float>& host) {
+  const Dims& D = X->D;
+  int half = D.hd / 2;
+  host.assign((size_t)D.max_len * D.hd, 0.f);
+  for (int t = 0; t < D.max_len; ++t)
+    for (int i = 0; i < half; ++i) {
+      double ang = (double)t * std::pow((double)D.theta, -2.0 * i / D.hd);
+      host[(size_t)t * D.hd + 2 * i] = (float)std::cos(ang);
+      host[(size_t)t * D.hd + 2 * i + 1] = (float)std::sin(ang);
+    }
+}
+
+}  // namespace
+
+// ======================================================================== C ABI
+
+extern "C" {
+
+size_t df_workspace_bytes(const df_config* cfg, size_t* kv_bytes) {
+  if (!valid_config(cfg, nullptr)) return 0;
+  Dims D = make_dims(cfg);
+  if (kv_bytes) *kv_bytes = kv_size(D);
+  return layout(D, nullptr, nullptr);
+}
+
+df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, void* workspace, void* cuda_stream,
+                    df_ctx** out) {
+  if (!out) return DF_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (!valid_config(cfg, &why)) {
+    fprintf(stderr, "df_create: %s\n", why.c_str());
+    return DF_ERR_ARG;
+  }
+  if (!w || !kv_buf || !workspace) return DF_ERR_ARG;
+  if (((uintptr_t)kv_buf & 255) || ((uintptr_t)workspace & 255)) return DF_ERR_ARG;
+  int L = cfg->n_layers;
+  if (!w->emb1 || !w->emb2 || !w->final_norm || !w->lm_head || !w->attn_norm || !w->wqkv || !w->wo ||
+      !w->mlp_norm || !w->wgu || !w->wd || !w->a || !w->b || !w->c)
+    return DF_ERR_ARG;
+  if (cfg->n_experts && !w->router) return DF_ERR_ARG;
+  for (int l = 0; l < L; ++l) {
+    if (!w->attn_norm[l] || !w->wqkv[l] || !w->wo[l] || !w->mlp_norm[l] || !w->wgu[l] || !w->wd[l] || !w->a[l] ||
+        !w->b[l] || !w->c[l])
+      return DF_ERR_ARG;
+    if (cfg->n_experts && !w->router[l]) return DF_ERR_ARG;
+  }
+  df_ctx* X = new df_ctx();
+  X->cfg = *cfg;
+  X->D = make_dims(cfg);
+  X->emb1 = w->emb1;
+  X->emb2 = w->emb2;
+  X->final_norm = w->final_norm;
+  X->lm_head = w->lm_head;
+  X->attn_norm.assign(w->attn_norm, w->attn_norm + L);
+  X->mlp_norm.assign(w->mlp_norm, w->mlp_norm + L);
+  X->wqkv.assign(w->wqkv, w->wqkv + L);
+  X->wo.assign(w->wo, w->wo + L);
+  X->wgu.assign(w->wgu, w->wgu + L);
+  X->wd.assign(w->wd, w->wd + L);
+  X->a.assign(w->a, w->a + L);
+  X->b.assign(w->b, w->b + L);
+  X->c.assign(w->c, w->c + L);
+  if (cfg->n_experts) X->router.assign(w->router, w->router + L);
+  X->kv = kv_buf;
+  X->ws = (char*)workspace;
+  size_t ws_bytes = layout(X->D, &X->Bf, X->ws);
+  if (cuda_stream) {
+    X->stream = (cudaStream_t)cuda_stream;
+  } else {
+    cudaError_t e = cudaStreamCreate(&X->stream);  // blocking: ordered with the legacy stream
+    if (e != cudaSuccess) {
+      delete X;
+      return DF_ERR_CUDA;
+    }
+    X->own_stream = true;
+  }
+  const char* ng = getenv("DF_NO_GRAPH");
+  X->use_graph = !(ng && ng[0] == '1');
+  const char* fg = getenv("DF_FORCE_GENERIC");
+  X->force_generic = (fg && fg[0] == '1') ? 1 : 0;
+  df::kernels_init();
+  std::vector<float> rope;
+  setup_rope(X, rope);
+  cudaError_t e = cudaMemsetAsync(X->ws, 0, ws_bytes, X->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(X->Bf.rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice, X->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(X->stream);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "df_create: %s\n", cudaGetErrorString(e));
+    if (X->own_stream) cudaStreamDestroy(X->stream);
+    delete X;
+    return DF_ERR_CUDA;
+  }
+  std::string perr;
+  if (!df::tc_plan_init(X->tc, X->D, X->Bf, X->wqkv, X->wo, X->wgu, X->wd, X->lm_head, &perr) ||
+      !df::attn_fast_init(X->at, X->D, X->kv, &perr)) {
+    fprintf(stderr, "df_create: %s\n", perr.c_str());
+    if (X->own_stream) cudaStreamDestroy(X->stream);
+    delete X;
+    return DF_ERR_CUDA;
+  }
+  *out = X;
+  return DF_OK;
+}
+
+static df_status set_batch(df_ctx* X, int B) {
+  if (B != X->B) {
+    X->dec.reset();
+    X->pre.reset();
+    X->B = B;
+    X->splits = df::attn_splits(X->D, B);
+    std::string perr;
+    if (!df::tc_plan_batch(X->tc, X->D, B, &perr)) return fail(X, DF_ERR_CUDA, perr);
+  }
+  return DF_OK;
+}
+
+df_status df_prefill(df_ctx* X, const int32_t* tokens, int B, int n) {
+  if (!X) return DF_ERR_ARG;
+  if (B <= 0 || n < 0 || (n > 0 && !tokens)) return fail(X, DF_ERR_ARG, "df_prefill: bad arguments");
+  if (B > X->cfg.max_batch) return fail(X, DF_ERR_CAPACITY, "df_prefill: B > max_batch");
+  if (n > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_prefill: n > max_len");
+  df_status st = set_batch(X, B);
+  if (st != DF_OK) return st;
+  df::launch_set_pos(X->Bf.ctrl, 0, X->stream);
+  X->t = 0;
+  X->ready = true;
+  if (n == 0) return DF_OK;
+  GraphKey key{};
+  key.p[0] = tokens;
+  key.i[0] = n;
+  key.i[1] = B;
+  key.i[2] = X->force_generic;
+  st = run_captured(X, X->pre, key, [&] { enqueue_prefill_pos(X, tokens, n); }, n);
+  if (st != DF_OK) return st;
+  X->t = n;
+  return DF_OK;
+}
+
+df_status df_set_length(df_ctx* X, int B, int t) {
+  if (!X) return DF_ERR_ARG;
+  if (B <= 0 || t < 0) return fail(X, DF_ERR_ARG, "df_set_length: bad arguments");
+  if (B > X->cfg.max_batch) return fail(X, DF_ERR_CAPACITY, "df_set_length: B > max_batch");
+  if (t > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_set_length: t > max_len");
+  df_status st = set_batch(X, B);
+  if (st != DF_OK) return st;
+  df::launch_set_pos(X->Bf.ctrl, t, X->stream);
+  X->t = t;
+  X->ready = true;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DF_OK : cuda_fail(X, e, "df_set_length");
+}
+
+df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax, float* alpha) {
+  if (!X) return DF_ERR_ARG;
+  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step: null tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step before df_prefill");
+  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step: cache full (t >= max_len)");
+  GraphKey key{};
+  key.p[0] = tokens;
+  key.p[1] = logp_mix;
+  key.p[2] = argmax;
+  key.p[3] = alpha;
+  key.p[4] = X->dbg_logp1;
+  key.p[5] = X->dbg_logp2;
+  key.p[6] = X->dbg_topk;
+  key.p[7] = X->dbg_router;
+  key.i[0] = X->aux_on;
+  key.i[1] = X->ungrouped;
+  key.i[2] = X->B;
+  key.i[3] = X->force_generic;
+  StepOut o{logp_mix, argmax, alpha};
+  df_status st = run_captured(X, X->dec, key, [&] { enqueue_decode(X, tokens, o); }, 1);
+  if (st != DF_OK) return st;
+  X->t += 1;
+  return DF_OK;
+}
+
+df_status df_sync(df_ctx* X) {
+  if (!X) return DF_ERR_ARG;
+  df::Ctrl h{};
+  cudaError_t e = cudaMemcpyAsync(&h, X->Bf.ctrl, sizeof(int) * 4, cudaMemcpyDeviceToHost, X->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_sync");
+  if (h.err) {
+    char buf[128];
+    snprintf(buf, sizeof(buf), "device error %d (detail %d)", h.err, h.err_info);
+    X->err = buf;
+    // the error is reported once; clear the latch so the context stays usable
+    cudaMemsetAsync(&X->Bf.ctrl->err, 0, 2 * sizeof(int), X->stream);
+    cudaStreamSynchronize(X->stream);
+    return (df_status)h.err;
+  }
+  return DF_OK;
+}
+
+df_status df_decode_step_host(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax, float* alpha) {
+  if (!X) return DF_ERR_ARG;
+  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_host: null tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_host before df_prefill");
+  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step_host: cache full");
+  int B = X->B, V = X->D.V;
+  cudaError_t e = cudaMemcpyAsync(X->Bf.tokbuf, tokens, B * sizeof(int32_t), cudaMemcpyHostToDevice, X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "token copy");
+  df_status st = df_decode_step(X, X->Bf.tokbuf, logp_mix ? X->Bf.out_logp : nullptr, argmax ? X->Bf.out_arg : nullptr,
+                                alpha ? X->Bf.out_alpha : nullptr);
+  if (st != DF_OK) return st;
+  if (logp_mix) e = cudaMemcpyAsync(logp_mix, X->Bf.out_logp, (size_t)B * V * 4, cudaMemcpyDeviceToHost, X->stream);
+  if (e == cudaSuccess && argmax) e = cudaMemcpyAsync(argmax, X->Bf.out_arg, B * 4, cudaMemcpyDeviceToHost, X->stream);
+  if (e == cudaSuccess && alpha) e = cudaMemcpyAsync(alpha, X->Bf.out_alpha, B * 4, cudaMemcpyDeviceToHost, X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "output copy");
+  return df_sync(X);
+}
+
+df_status df_set_mode(df_ctx* X, int aux_on, int ungrouped) {
+  if (!X) return DF_ERR_ARG;
+  if ((aux_on != 0 && aux_on != 1) || (ungrouped != 0 && ungrouped != 1))
+    return fail(X, DF_ERR_ARG, "df_set_mode: flags must be 0 or 1");
+  X->aux_on = aux_on;
+  X->ungrouped = ungrouped;
+  return DF_OK;
+}
+
+df_status df_debug_outputs(df_ctx* X, float* logp1, float* logp2, int32_t* topk, float* router) {
+  if (!X) return DF_ERR_ARG;
+  if ((topk || router) && !X->cfg.n_experts) return fail(X, DF_ERR_ARG, "topk/router diagnostics need an MoE model");
+  X->dbg_logp1 = logp1;
+  X->dbg_logp2 = logp2;
+  X->dbg_topk = topk;
+  X->dbg_router = router;
+  return DF_OK;
+}
+
+df_status df_time_op(df_ctx* X, int op, int iters, float* avg_ms) {
+  if (!X || !avg_ms || iters <= 0) return DF_ERR_ARG;
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_time_op before df_prefill");
+  if (op < 0 || op > DF_OP_MOE) return fail(X, DF_ERR_ARG, "df_time_op: unknown op");
+  if (op == DF_OP_MOE && !X->D.E) return fail(X, DF_ERR_ARG, "df_time_op: MoE op on a dense model");
+  if ((op == DF_OP_GATEUP || op == DF_OP_DOWN) && X->D.E) return fail(X, DF_ERR_ARG, "df_time_op: dense op on MoE");
+  int B = X->B;
+  Rows R{B, 0, X->aux_on ? 2 * B : B};
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  cudaEventRecord(e0, X->stream);
+  for (int i = 0; i < iters; ++i) {
+    int l = i % X->D.L;
+    Couple C = layer_couple(X, l, 0, 0);
+    switch (op) {
+      case DF_OP_QKV: op_qkv(X, l, R, C); break;
+      case DF_OP_ATTN: op_attn(X, l, R); break;
+      case DF_OP_WO: op_wo(X, l, R); break;
+      case DF_OP_GATEUP: op_gateup(X, l, R, C); break;
+      case DF_OP_DOWN: op_down(X, l, R, C); break;
+      case DF_OP_LMHEAD: op_lm(X, R); break;
+      case DF_OP_MOE: op_moe(X, l, R, C); break;
+    }
+  }
+  cudaEventRecord(e1, X->stream);
+  cudaError_t e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_time_op");
+  *avg_ms = ms / iters;
+  return DF_OK;
+}
+
+int df_length(const df_ctx* X) { return X ? X->t : -1; }
+
+int df_step_kernels(const df_ctx* X) { return X ? X->last_kernels : -1; }
+
+const char* df_last_error(const df_ctx* X) { return X ? X->err.c_str() : "null context"; }
+
+void df_destroy(df_ctx* X) {
+  if (!X) return;
+  if (X->stream) cudaStreamSynchronize(X->stream);
+  X->dec.reset();
+  X->pre.reset();
+  df::tc_plan_free(X->tc);
+  df::attn_fast_free(X->at);
+  if (X->own_stream) cudaStreamDestroy(X->stream);
+  delete X;
+}
+
+}  // extern "C"

@@ -1,0 +1,741 @@
+// CUDA-core kernels of the dual-flow decode step: embedding stack, RMSNorm,
+// GEMV, the fused GEMM epilogues (QKV + coupling + RoPE + cache append,
+// SwiGLU + b coupling, down + c coupling + residual), split-KV attention for
+// any head size, the split merge, the softmax/mixture head and the MoE
+// router-replay pieces.
+//
+// Method source: "Resumen Técnico: Dual-Flow Transformers" (gist.science),
+// sections "Arquitectura Central" and "Mecanismos Clave".  Stacked rows:
+// 0..B-1 primary flow, B..2B-1 auxiliary flow (same sequence order).
+
+#include <math.h>
+
+#include "df_internal.h"
+
+namespace df {
+
+// ------------------------------------------------------------------ position
+
+__global__ void k_set_pos(Ctrl* c, int t) { c->t = t; }
+__global__ void k_advance_pos(Ctrl* c) { c->t += 1; }
+
+template <typename T>
+__global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
+                               const Ctrl* __restrict__ ctrl, float* __restrict__ part_o,
+                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
+                               int splits, int flo, int fhi);
+
+void kernels_init() {
+  cudaFuncSetAttribute(k_attn_generic<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(k_attn_generic<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { k_set_pos<<<1, 1, 0, s>>>(c, t); }
+void launch_advance_pos(Ctrl* c, cudaStream_t s) { k_advance_pos<<<1, 1, 0, s>>>(c); }
+
+// ------------------------------------------------------------------ embedding
+// h[b] = E1[x_b], h[B+b] = E2[x_b]: the two flows use separate token
+// embeddings of the same token ("Arquitectura Central", Separación).
+
+template <typename T>
+__global__ void k_embed(const T* __restrict__ e1, const T* __restrict__ e2, const int32_t* __restrict__ tok,
+                        int tok_stride, int use_pos, Ctrl* ctrl, float* __restrict__ h, int B, int lo, int d,
+                        int V) {
+  int m = lo + blockIdx.x;
+  int f = m >= B, b = m - f * B;
+  int idx = b * tok_stride + (use_pos ? ctrl->t : 0);
+  int id = tok[idx];
+  bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) latch_error(ctrl, kErrDevice, 1000 + b);
+  const T* e = (f ? e2 : e1) + (size_t)(ok ? id : 0) * d;
+  float* out = h + (size_t)m * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) out[i] = ok ? Num<T>::to_f(e[i]) : 0.f;
+}
+
+void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void* emb2, const int32_t* tokens,
+                  int tok_stride, int use_pos, const Rows& R, cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  if (D.bf16)
+    k_embed<__nv_bfloat16><<<n, 256, 0, s>>>((const __nv_bfloat16*)emb1, (const __nv_bfloat16*)emb2, tokens,
+                                              tok_stride, use_pos, Bf.ctrl, Bf.h, R.B, R.lo, D.d, D.V);
+  else
+    k_embed<float><<<n, 256, 0, s>>>((const float*)emb1, (const float*)emb2, tokens, tok_stride, use_pos,
+                                     Bf.ctrl, Bf.h, R.B, R.lo, D.d, D.V);
+}
+
+// ------------------------------------------------------------------ RMSNorm
+// u = x / sqrt(mean(x^2) + eps) * g, rounded to the storage type for the
+// next GEMM; optionally also kept unrounded in fp32 (MoE router input).
+
+template <typename T>
+__global__ void k_rmsnorm(const float* __restrict__ h, const float* __restrict__ g, T* __restrict__ out,
+                          float* __restrict__ out_f32, int d, float eps, int lo) {
+  __shared__ float red[32];
+  int m = lo + blockIdx.x;
+  const float* x = h + (size_t)m * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) ss += x[i] * x[i];
+  ss = block_sum(ss, red);
+  float r = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = x[i] * r * g[i];
+    out[(size_t)m * d + i] = Num<T>::from_f(v);
+    if (out_f32) out_f32[(size_t)m * d + i] = v;
+  }
+}
+
+void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out, float* out_f32, const Rows& R,
+                    cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  if (D.bf16)
+    k_rmsnorm<__nv_bfloat16><<<n, 256, 0, s>>>(Bf.h, g, (__nv_bfloat16*)out, out_f32, D.d, D.eps, R.lo);
+  else
+    k_rmsnorm<float><<<n, 256, 0, s>>>(Bf.h, g, (float*)out, out_f32, D.d, D.eps, R.lo);
+}
+
+// ------------------------------------------------------------------ GEMV (CUDA cores)
+// One warp per output feature; lanes stride the reduction dimension with
+// coalesced loads; rows are processed R at a time with one accumulator each.
+// Each row's sum depends only on that row, so results do not change with the
+// set of active rows.
+
+template <typename TW, typename TX, int R>
+__global__ void k_gemv(const TW* __restrict__ W, int N, int K, const TX* __restrict__ X, int ldx,
+                       float* __restrict__ out, int ldo, int lo, int hi) {
+  int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int n = blockIdx.x * warps + w; n < N; n += gridDim.x * warps) {
+    const TW* wr = W + (size_t)n * K;
+    for (int r0 = lo; r0 < hi; r0 += R) {
+      float acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = 0.f;
+      for (int k = lane; k < K; k += 32) {
+        float wv = Num<TW>::to_f(wr[k]);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (r0 + r < hi) acc[r] = fmaf(wv, Num<TX>::to_f(X[(size_t)(r0 + r) * ldx + k]), acc[r]);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float v = warp_sum(acc[r]);
+        if (lane == 0 && r0 + r < hi) out[(size_t)(r0 + r) * ldo + n] = v;
+      }
+    }
+  }
+}
+
+void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, int x_f32, float* out,
+                 int ldo, const Rows& R, cudaStream_t s) {
+  if (R.hi <= R.lo || N <= 0) return;
+  int blocks = (N + 7) / 8;
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  if (D.bf16) {
+    if (x_f32)
+      k_gemv<__nv_bfloat16, float, 8><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)W, N, K, (const float*)X, ldx,
+                                                              out, ldo, R.lo, R.hi);
+    else
+      k_gemv<__nv_bfloat16, __nv_bfloat16, 8><<<blocks, 256, 0, s>>>(
+          (const __nv_bfloat16*)W, N, K, (const __nv_bfloat16*)X, ldx, out, ldo, R.lo, R.hi);
+  } else {
+    k_gemv<float, float, 8><<<blocks, 256, 0, s>>>((const float*)W, N, K, (const float*)X, ldx, out, ldo, R.lo,
+                                                   R.hi);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+// QKV epilogue ("Mecanismos Clave", Atención de KV Compartido Asimétrico):
+//  primary row b:   q1 = raw[b][0:qdim] (pre-RoPE), K/V of position t are
+//                   RoPE(k1), v1 rounded to the cache type and appended;
+//  auxiliary row:   Q2 = raw[B+b][0:qdim] + a ⊙ q1 (coupling before RoPE); its
+//                   own K/V columns are discarded (the auxiliary flow writes
+//                   no cache);
+//  both:            the rotated query is rounded to the cache type.
+
+template <typename T>
+__global__ void k_ep_qkv(const float* __restrict__ raw, int ldr, const float* __restrict__ a, T* __restrict__ kvl,
+                         const float* __restrict__ rope, const Ctrl* __restrict__ ctrl, float* __restrict__ qatt,
+                         Couple C, int B, int lo, int Hq, int Hkv, int hd, int maxB, int max_len) {
+  int m = lo + blockIdx.x;
+  int f = m >= B, b = m - f * B;
+  int t = ctrl->t;
+  int half = hd >> 1, qdim = Hq * hd, kvdim = Hkv * hd;
+  const float* cs = rope + (size_t)t * hd;
+  const float* rr = raw + (size_t)m * ldr;
+  for (int p = threadIdx.x; p < Hq * half; p += blockDim.x) {
+    int n0 = (p / half) * hd + (p % half), n1 = n0 + half, i = p % half;
+    float v0 = rr[n0], v1 = rr[n1];
+    if (f) {
+      float p0, p1;
+      if (C.saved) {
+        p0 = C.q1s[(size_t)b * qdim + n0];
+        p1 = C.q1s[(size_t)b * qdim + n1];
+      } else {
+        p0 = raw[(size_t)b * ldr + n0];
+        p1 = raw[(size_t)b * ldr + n1];
+      }
+      v0 = fmaf(a[n0], p0, v0);
+      v1 = fmaf(a[n1], p1, v1);
+    } else if (C.save) {
+      C.q1s[(size_t)b * qdim + n0] = v0;
+      C.q1s[(size_t)b * qdim + n1] = v1;
+    }
+    float c = cs[2 * i], s = cs[2 * i + 1];
+    qatt[(size_t)m * qdim + n0] = Num<T>::quant(v0 * c - v1 * s);
+    qatt[(size_t)m * qdim + n1] = Num<T>::quant(v1 * c + v0 * s);
+  }
+  if (f) return;
+  size_t vbase = (size_t)maxB * Hkv * max_len * hd;  // V half of the layer block
+  for (int p = threadIdx.x; p < Hkv * half; p += blockDim.x) {
+    int g = p / half, i = p % half;
+    float k0 = rr[qdim + g * hd + i], k1 = rr[qdim + g * hd + i + half];
+    float c = cs[2 * i], s = cs[2 * i + 1];
+    T* Kp = kvl + (((size_t)b * Hkv + g) * max_len + t) * hd;
+    Kp[i] = Num<T>::from_f(k0 * c - k1 * s);
+    Kp[i + half] = Num<T>::from_f(k1 * c + k0 * s);
+  }
+  for (int p = threadIdx.x; p < kvdim; p += blockDim.x) {
+    int g = p / hd, i = p % hd;
+    T* Vp = kvl + vbase + (((size_t)b * Hkv + g) * max_len + t) * hd;
+    Vp[i] = Num<T>::from_f(rr[qdim + kvdim + p]);
+  }
+}
+
+void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* a, void* kv, int layer,
+                   const Couple& C, const Rows& R, cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
+  if (D.bf16)
+    k_ep_qkv<__nv_bfloat16><<<n, 256, 0, s>>>(raw, ldr, a, (__nv_bfloat16*)kv + layer * layer_elems, Bf.rope,
+                                               Bf.ctrl, Bf.qatt, C, R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB,
+                                               D.max_len);
+  else
+    k_ep_qkv<float><<<n, 256, 0, s>>>(raw, ldr, a, (float*)kv + layer * layer_elems, Bf.rope, Bf.ctrl, Bf.qatt, C,
+                                      R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB, D.max_len);
+}
+
+// SwiGLU epilogue with the MLP-intermediate coupling ("Mecanismos Clave",
+// Acoplamiento Ligero): z = silu(gate) ⊙ up; auxiliary rows add b ⊙ z1.
+// Gate/up rows are interleaved in blocks of 64 (see df_weights.wgu).
+template <typename T>
+__global__ void k_ep_swiglu(const float* __restrict__ raw, int ldr, const float* __restrict__ bvec,
+                            T* __restrict__ z, Couple C, int B, int lo, int F) {
+  int m = lo + blockIdx.x;
+  int f = m >= B, b = m - f * B;
+  for (int fi = threadIdx.x; fi < F; fi += blockDim.x) {
+    int ng = (fi >> 6) * 128 + (fi & 63), nu = ng + 64;
+    float zz = silu_f(raw[(size_t)m * ldr + ng]) * raw[(size_t)m * ldr + nu];
+    if (f) {
+      float z1 = C.saved ? C.z1s[(size_t)b * F + fi]
+                         : silu_f(raw[(size_t)b * ldr + ng]) * raw[(size_t)b * ldr + nu];
+      zz = fmaf(bvec[fi], z1, zz);
+    } else if (C.save) {
+      C.z1s[(size_t)b * F + fi] = zz;
+    }
+    z[(size_t)m * F + fi] = Num<T>::from_f(zz);
+  }
+}
+
+void launch_ep_swiglu(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* bvec,
+                      const Couple& C, const Rows& R, cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  if (D.bf16)
+    k_ep_swiglu<__nv_bfloat16><<<n, 256, 0, s>>>(raw, ldr, bvec, (__nv_bfloat16*)Bf.z, C, R.B, R.lo, D.F);
+  else
+    k_ep_swiglu<float><<<n, 256, 0, s>>>(raw, ldr, bvec, (float*)Bf.z, C, R.B, R.lo, D.F);
+}
+
+// Down-projection epilogue with the MLP-output coupling: y2 += c ⊙ y1, then
+// the residual add h += y for both flows.
+__global__ void k_ep_down(const float* __restrict__ raw, int ldr, const float* __restrict__ cvec,
+                          float* __restrict__ h, Couple C, int B, int lo, int d) {
+  int m = lo + blockIdx.x;
+  int f = m >= B, b = m - f * B;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+    float y = raw[(size_t)m * ldr + n];
+    if (f) {
+      float y1 = C.saved ? C.y1s[(size_t)b * d + n] : raw[(size_t)b * ldr + n];
+      y = fmaf(cvec[n], y1, y);
+    } else if (C.save) {
+      C.y1s[(size_t)b * d + n] = y;
+    }
+    h[(size_t)m * d + n] += y;
+  }
+}
+
+void launch_ep_down(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* cvec,
+                    const Couple& C, const Rows& R, cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  k_ep_down<<<n, 256, 0, s>>>(raw, ldr, cvec, Bf.h, C, R.B, R.lo, D.d);
+}
+
+__global__ void k_ep_residual(const float* __restrict__ raw, int ldr, float* __restrict__ h, int lo, int d) {
+  int m = lo + blockIdx.x;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) h[(size_t)m * d + n] += raw[(size_t)m * ldr + n];
+}
+
+void launch_ep_residual(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const Rows& R,
+                        cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  k_ep_residual<<<n, 256, 0, s>>>(raw, ldr, Bf.h, R.lo, D.d);
+}
+
+// ------------------------------------------------------------------ attention
+// Split-KV decode attention over the primary cache positions 0..t, shared by
+// the primary queries and the auxiliary queries of the same KV head
+// ("Mecanismos Clave": the auxiliary flow attends to K1, V1).  Grid: (split,
+// kv head, sequence).  Each split keeps a running max m, running sum l and
+// unnormalised output o per query row; attn_combine merges the splits.
+// Partial slot of a query row: ((b*Hkv + g)*splits + s)*2G + f*G + j.
+
+int attn_splits(const Dims& D, int B) {
+  int pairs = B * D.Hkv;
+  int want = (2 * 148 + pairs - 1) / pairs;
+  int maxs = (D.max_len + 63) / 64;
+  if (want > maxs) want = maxs;
+  if (want < 1) want = 1;
+  return want;
+}
+
+__device__ __forceinline__ void split_range(int n, int splits, int s, int& s0, int& s1) {
+  int chunk = (n + splits - 1) / splits;
+  chunk = (chunk + 63) & ~63;
+  s0 = s * chunk;
+  s1 = min(n, s0 + chunk);
+}
+
+template <typename T>
+__global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
+                               const Ctrl* __restrict__ ctrl, float* __restrict__ part_o,
+                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
+                               int splits, int flo, int fhi) {
+  constexpr int CH = 128;  // positions per chunk == blockDim.x
+  extern __shared__ float sm[];
+  int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  int Ract = (fhi - flo) * G;
+  int qdim = Hkv * G * hd;
+  float* q = sm;                        // [Ract][hd]
+  float* o = q + Ract * hd;             // [Ract][hd]
+  float* sc = o + Ract * hd;            // [Ract][CH]
+  float* mrow = sc + Ract * CH;         // [Ract]
+  float* lrow = mrow + Ract;
+  float* corr = lrow + Ract;
+  int n = ctrl->t + 1;
+  int s0, s1;
+  split_range(n, splits, s, s0, s1);
+  const T* K = kvl + ((size_t)b * Hkv + g) * max_len * hd;
+  const T* V = kvl + (size_t)maxB * Hkv * max_len * hd + ((size_t)b * Hkv + g) * max_len * hd;
+  float scale = 1.0f / sqrtf((float)hd);
+  for (int idx = threadIdx.x; idx < Ract * hd; idx += blockDim.x) {
+    int r = idx / hd, i = idx % hd;
+    int f = flo + r / G, j = r % G;
+    q[idx] = qatt[(size_t)(f * B + b) * qdim + (g * G + j) * hd + i];
+    o[idx] = 0.f;
+  }
+  for (int r = threadIdx.x; r < Ract; r += blockDim.x) {
+    mrow[r] = -INFINITY;
+    lrow[r] = 0.f;
+  }
+  __syncthreads();
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int c0 = s0; c0 < s1; c0 += CH) {
+    int pos = c0 + threadIdx.x;
+    if (pos < s1) {
+      const T* kr = K + (size_t)pos * hd;
+      for (int r = 0; r < Ract; ++r) {
+        float dot = 0.f;
+        for (int i = 0; i < hd; ++i) dot = fmaf(q[r * hd + i], Num<T>::to_f(kr[i]), dot);
+        sc[r * CH + threadIdx.x] = dot * scale;
+      }
+    } else {
+      for (int r = 0; r < Ract; ++r) sc[r * CH + threadIdx.x] = -INFINITY;
+    }
+    __syncthreads();
+    for (int r = w; r < Ract; r += nw) {
+      float mx = -INFINITY;
+      for (int j = lane; j < CH; j += 32) mx = fmaxf(mx, sc[r * CH + j]);
+      mx = warp_max(mx);
+      float mnew = fmaxf(mrow[r], mx);
+      float cf = (mrow[r] == -INFINITY) ? 0.f : expf(mrow[r] - mnew);
+      float sum = 0.f;
+      for (int j = lane; j < CH; j += 32) {
+        float p = (sc[r * CH + j] == -INFINITY) ? 0.f : expf(sc[r * CH + j] - mnew);
+        sc[r * CH + j] = p;
+        sum += p;
+      }
+      sum = warp_sum(sum);
+      __syncwarp();
+      if (lane == 0) {
+        lrow[r] = lrow[r] * cf + sum;
+        mrow[r] = mnew;
+        corr[r] = cf;
+      }
+    }
+    __syncthreads();
+    int cnt = min(CH, s1 - c0);
+    for (int idx = threadIdx.x; idx < Ract * hd; idx += blockDim.x) {
+      int r = idx / hd, i = idx % hd;
+      float acc = o[idx] * corr[r];
+      for (int j = 0; j < cnt; ++j) acc = fmaf(sc[r * CH + j], Num<T>::to_f(V[(size_t)(c0 + j) * hd + i]), acc);
+      o[idx] = acc;
+    }
+    __syncthreads();
+  }
+  size_t slot0 = ((size_t)(b * Hkv + g) * splits + s) * (2 * G) + flo * G;
+  for (int idx = threadIdx.x; idx < Ract * hd; idx += blockDim.x) part_o[slot0 * hd + idx] = o[idx];
+  for (int r = threadIdx.x; r < Ract; r += blockDim.x) {
+    part_ml[(slot0 + r) * 2 + 0] = mrow[r];
+    part_ml[(slot0 + r) * 2 + 1] = lrow[r];
+  }
+}
+
+void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, int layer, int splits,
+                              const Rows& R, cudaStream_t s) {
+  int flo = R.lo >= R.B ? 1 : 0, fhi = R.hi > R.B ? 2 : 1;
+  int Ract = (fhi - flo) * D.G;
+  size_t smem = (size_t)(Ract * (2 * D.hd + 128) + 3 * Ract) * sizeof(float);
+  dim3 grid(splits, D.Hkv, R.B);
+  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
+  if (D.bf16) {
+    k_attn_generic<__nv_bfloat16><<<grid, 128, smem, s>>>((const __nv_bfloat16*)kv + layer * layer_elems, Bf.qatt,
+                                                          Bf.ctrl, Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd,
+                                                          D.maxB, D.max_len, splits, flo, fhi);
+  } else {
+    k_attn_generic<float><<<grid, 128, smem, s>>>((const float*)kv + layer * layer_elems, Bf.qatt, Bf.ctrl,
+                                                  Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd, D.maxB, D.max_len,
+                                                  splits, flo, fhi);
+  }
+}
+
+// Merge of split partials: o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s,
+// in split order, rounded to the GEMM input type.
+template <typename T>
+__global__ void k_attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                               T* __restrict__ out, int B, int Hkv, int G, int hd, int splits, int flo) {
+  int b = blockIdx.x, head = blockIdx.y, f = flo + blockIdx.z;
+  int g = head / G, j = head % G;
+  int qdim = Hkv * G * hd;
+  size_t base = (size_t)(b * Hkv + g) * splits * (2 * G) + f * G + j;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_ml[(base + (size_t)s * 2 * G) * 2]);
+  float den = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    float ms = part_ml[(base + (size_t)s * 2 * G) * 2];
+    if (ms != -INFINITY) den += expf(ms - M) * part_ml[(base + (size_t)s * 2 * G) * 2 + 1];
+  }
+  float inv = 1.0f / den;
+  for (int i = threadIdx.x; i < hd; i += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      size_t slot = base + (size_t)s * 2 * G;
+      float ms = part_ml[slot * 2];
+      if (ms != -INFINITY) acc = fmaf(expf(ms - M), part_o[slot * hd + i], acc);
+    }
+    out[(size_t)(f * B + b) * qdim + head * hd + i] = Num<T>::from_f(acc * inv);
+  }
+}
+
+void launch_attn_combine(const Dims& D, const Buffers& Bf, int splits, const Rows& R, cudaStream_t s) {
+  int flo = R.lo >= R.B ? 1 : 0, fhi = R.hi > R.B ? 2 : 1;
+  dim3 grid(R.B, D.Hq, fhi - flo);
+  if (D.bf16)
+    k_attn_combine<__nv_bfloat16><<<grid, 128, 0, s>>>(Bf.part_o, Bf.part_ml, (__nv_bfloat16*)Bf.o, R.B, D.Hkv,
+                                                        D.G, D.hd, splits, flo);
+  else
+    k_attn_combine<float><<<grid, 128, 0, s>>>(Bf.part_o, Bf.part_ml, (float*)Bf.o, R.B, D.Hkv, D.G, D.hd, splits,
+                                               flo);
+}
+
+// ------------------------------------------------------------------ mixture head
+// p1 = softmax(l1), p2 = softmax(l2), alpha = 0.5 + 0.5 * sum p1^2 (the
+// primary's collision probability, so alpha >= 1/2), log p_mix =
+// logaddexp(log alpha + log p1, log(1 - alpha) + log p2), argmax with the
+// lowest index among equal values ("Mecanismos Clave", Objetivo de Mezcla).
+
+__device__ __forceinline__ float logaddexp_f(float x, float y) {
+  if (x == -INFINITY) return y;
+  if (y == -INFINITY) return x;
+  float mx = fmaxf(x, y), mn = fminf(x, y);
+  return mx + log1pf(expf(mn - mx));
+}
+
+__global__ void k_mix(const float* __restrict__ logits, int B, int V, int aux_on, float* __restrict__ logp_mix,
+                      int32_t* __restrict__ argmax, float* __restrict__ alpha_out, float* __restrict__ logp1,
+                      float* __restrict__ logp2) {
+  __shared__ float red[32];
+  __shared__ float redv[32];
+  __shared__ int redi[32];
+  int b = blockIdx.x;
+  const float* l1 = logits + (size_t)b * V;
+  const float* l2 = logits + (size_t)(B + b) * V;
+  float m1 = -INFINITY, m2 = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    m1 = fmaxf(m1, l1[v]);
+    if (aux_on) m2 = fmaxf(m2, l2[v]);
+  }
+  m1 = block_max(m1, red);
+  if (aux_on) m2 = block_max(m2, red);
+  float s1 = 0.f, q1 = 0.f, s2 = 0.f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    float e = expf(l1[v] - m1);
+    s1 += e;
+    q1 += e * e;
+    if (aux_on) s2 += expf(l2[v] - m2);
+  }
+  s1 = block_sum(s1, red);
+  q1 = block_sum(q1, red);
+  if (aux_on) s2 = block_sum(s2, red);
+  float lse1 = m1 + logf(s1);
+  float lse2 = aux_on ? m2 + logf(s2) : 0.f;
+  float coll = q1 / (s1 * s1);
+  float alpha = aux_on ? 0.5f + 0.5f * coll : 1.0f;
+  float la = logf(alpha);
+  float lb = (alpha < 1.0f) ? log1pf(-alpha) : -INFINITY;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    float lp1 = l1[v] - lse1;
+    float lm = lp1;
+    if (aux_on) {
+      float lp2 = l2[v] - lse2;
+      lm = logaddexp_f(la + lp1, lb + lp2);
+      if (logp2) logp2[(size_t)b * V + v] = lp2;
+    }
+    if (logp1) logp1[(size_t)b * V + v] = lp1;
+    if (logp_mix) logp_mix[(size_t)b * V + v] = lm;
+    if (lm > best) {
+      best = lm;
+      bi = v;
+    }
+  }
+  // block argmax: larger value wins, equal values -> lower index
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    redv[w] = best;
+    redi[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    best = lane < nw ? redv[lane] : -INFINITY;
+    bi = lane < nw ? redi[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      if (argmax) argmax[b] = bi;
+      if (alpha_out) alpha_out[b] = alpha;
+    }
+  }
+}
+
+void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax, float* alpha,
+                float* logp1, float* logp2, cudaStream_t s) {
+  k_mix<<<B, 1024, 0, s>>>(Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
+}
+
+// ------------------------------------------------------------------ MoE (router replay)
+// The primary rows choose their top-k experts (descending router logit,
+// ties to the lower index); each flow's gates are the softmax of its own
+// router logits over that set ("Mecanismos Clave", Replay de Router).  The
+// per-expert entry lists (b*k + j, ascending b) let every selected expert's
+// weights be read once for both flows.
+
+__global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, float* __restrict__ gate,
+                            int* __restrict__ ecount, int* __restrict__ elist, int B, int E, int k, int maxB,
+                            int select, int prim, int aux, int32_t* __restrict__ dbg_topk_l,
+                            float* __restrict__ dbg_router_l) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    if (select) {
+      const float* r = rlog + (size_t)b * E;
+      for (int j = 0; j < k; ++j) {
+        float best = -INFINITY;
+        int bi = -1;
+        for (int e = 0; e < E; ++e) {
+          bool taken = false;
+          for (int jj = 0; jj < j; ++jj) taken |= (topk_l[b * k + jj] == e);
+          if (taken) continue;
+          if (bi < 0 || r[e] > best) {
+            best = r[e];
+            bi = e;
+          }
+        }
+        topk_l[b * k + j] = bi;
+      }
+    }
+    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+      const float* r = rlog + (size_t)(f * B + b) * E;
+      float mx = -INFINITY;
+      for (int j = 0; j < k; ++j) mx = fmaxf(mx, r[topk_l[b * k + j]]);
+      float den = 0.f;
+      for (int j = 0; j < k; ++j) den += expf(r[topk_l[b * k + j]] - mx);
+      for (int j = 0; j < k; ++j) gate[(size_t)(f * B + b) * k + j] = expf(r[topk_l[b * k + j]] - mx) / den;
+    }
+    if (dbg_topk_l && prim)
+      for (int j = 0; j < k; ++j) dbg_topk_l[b * k + j] = topk_l[b * k + j];
+    if (dbg_router_l && prim)
+      for (int e = 0; e < E; ++e) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int cnt = 0;
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < k; ++j)
+        if (topk_l[b * k + j] == e) elist[(size_t)e * maxB + cnt++] = b * k + j;
+    ecount[e] = cnt;
+  }
+}
+
+void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
+                      float* dbg_router, cudaStream_t s) {
+  int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
+  k_moe_route<<<1, 256, 0, s>>>(Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, R.B, D.E, D.k, D.maxB, select,
+                                R.has_primary(), R.has_aux(),
+                                dbg_topk ? dbg_topk + (size_t)layer * R.B * D.k : nullptr,
+                                dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);
+}
+
+// Expert gate/up + SwiGLU + b coupling (CUDA cores): one warp per expert
+// hidden unit, looping over the expert's entries and the active flows.
+template <typename T>
+__global__ void k_moe_gateup(const T* __restrict__ wgu, const float* __restrict__ bvec, const T* __restrict__ u,
+                             const int* __restrict__ ecount, const int* __restrict__ elist, T* __restrict__ zE,
+                             Couple C, int B, int d, int Fe, int k, int maxB, int prim, int aux) {
+  int e = blockIdx.x;
+  int cnt = ecount[e];
+  if (cnt == 0) return;
+  int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int fi = blockIdx.y * warps + w;
+  if (fi >= Fe) return;
+  const T* W = wgu + (size_t)e * 2 * Fe * d;
+  const T* wg = W + (size_t)((fi >> 6) * 128 + (fi & 63)) * d;
+  const T* wu = wg + (size_t)64 * d;
+  for (int idx = 0; idx < cnt; ++idx) {
+    int ent = elist[(size_t)e * maxB + idx];
+    int b = ent / k, j = ent % k;
+    float z1 = 0.f;
+    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+      const T* x = u + (size_t)(f * B + b) * d;
+      float ag = 0.f, au = 0.f;
+      for (int kk = lane; kk < d; kk += 32) {
+        float xv = Num<T>::to_f(x[kk]);
+        ag = fmaf(Num<T>::to_f(wg[kk]), xv, ag);
+        au = fmaf(Num<T>::to_f(wu[kk]), xv, au);
+      }
+      ag = warp_sum(ag);
+      au = warp_sum(au);
+      float zz = silu_f(ag) * au;
+      if (f == 0) {
+        z1 = zz;
+        if (C.save && lane == 0) C.z1s[(size_t)ent * Fe + fi] = zz;
+      } else {
+        float p = C.saved ? C.z1s[(size_t)ent * Fe + fi] : z1;
+        zz = fmaf(bvec[fi], p, zz);
+      }
+      if (lane == 0) zE[((size_t)(f * maxB + b) * k + j) * Fe + fi] = Num<T>::from_f(zz);
+    }
+  }
+}
+
+void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu, const float* bvec,
+                               const Couple& C, const Rows& R, cudaStream_t s) {
+  dim3 grid(D.E, (D.Fe + 7) / 8);
+  if (D.bf16)
+    k_moe_gateup<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)wgu, bvec, (const __nv_bfloat16*)Bf.u,
+                                                      Bf.ecount, Bf.elist, (__nv_bfloat16*)Bf.zE, C, R.B, D.d,
+                                                      D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
+  else
+    k_moe_gateup<float><<<grid, 256, 0, s>>>((const float*)wgu, bvec, (const float*)Bf.u, Bf.ecount, Bf.elist,
+                                             (float*)Bf.zE, C, R.B, D.d, D.Fe, D.k, D.maxB, R.has_primary(),
+                                             R.has_aux());
+}
+
+template <typename T>
+__global__ void k_moe_down(const T* __restrict__ wd, const T* __restrict__ zE, const int* __restrict__ ecount,
+                           const int* __restrict__ elist, float* __restrict__ yE, int d, int Fe, int k, int maxB,
+                           int prim, int aux) {
+  int e = blockIdx.x;
+  int cnt = ecount[e];
+  if (cnt == 0) return;
+  int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int n = blockIdx.y * warps + w;
+  if (n >= d) return;
+  const T* wr = wd + ((size_t)e * d + n) * Fe;
+  for (int idx = 0; idx < cnt; ++idx) {
+    int ent = elist[(size_t)e * maxB + idx];
+    int b = ent / k, j = ent % k;
+    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+      const T* z = zE + ((size_t)(f * maxB + b) * k + j) * Fe;
+      float acc = 0.f;
+      for (int kk = lane; kk < Fe; kk += 32) acc = fmaf(Num<T>::to_f(wr[kk]), Num<T>::to_f(z[kk]), acc);
+      acc = warp_sum(acc);
+      if (lane == 0) yE[((size_t)(f * maxB + b) * k + j) * d + n] = acc;
+    }
+  }
+}
+
+void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, const Rows& R, cudaStream_t s) {
+  dim3 grid(D.E, (D.d + 7) / 8);
+  if (D.bf16)
+    k_moe_down<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)wd, (const __nv_bfloat16*)Bf.zE,
+                                                    Bf.ecount, Bf.elist, Bf.yE, D.d, D.Fe, D.k, D.maxB,
+                                                    R.has_primary(), R.has_aux());
+  else
+    k_moe_down<float><<<grid, 256, 0, s>>>((const float*)wd, (const float*)Bf.zE, Bf.ecount, Bf.elist, Bf.yE, D.d,
+                                           D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
+}
+
+// y_f = sum_j gate_f[j] * yE_f[j] (slot order), y2 += c ⊙ y1, h += y.
+__global__ void k_moe_combine(const float* __restrict__ yE, const float* __restrict__ gate,
+                              const float* __restrict__ cvec, float* __restrict__ h, Couple C, int B, int lo, int d,
+                              int k, int maxB) {
+  int m = lo + blockIdx.x;
+  int f = m >= B, b = m - f * B;
+  for (int n = threadIdx.x; n < d; n += blockDim.x) {
+    float y = 0.f;
+    for (int j = 0; j < k; ++j)
+      y = fmaf(gate[(size_t)m * k + j], yE[((size_t)(f * maxB + b) * k + j) * d + n], y);
+    if (f) {
+      float y1;
+      if (C.saved) {
+        y1 = C.y1s[(size_t)b * d + n];
+      } else {
+        y1 = 0.f;
+        for (int j = 0; j < k; ++j) y1 = fmaf(gate[(size_t)b * k + j], yE[((size_t)b * k + j) * d + n], y1);
+      }
+      y = fmaf(cvec[n], y1, y);
+    } else if (C.save) {
+      C.y1s[(size_t)b * d + n] = y;
+    }
+    h[(size_t)m * d + n] += y;
+  }
+}
+
+void launch_moe_combine(const Dims& D, const Buffers& Bf, const float* cvec, const Couple& C, const Rows& R,
+                        cudaStream_t s) {
+  int n = R.hi - R.lo;
+  if (n <= 0) return;
+  k_moe_combine<<<n, 256, 0, s>>>(Bf.yE, Bf.gate, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.maxB);
+}
+
+}  // namespace df

@@ -1,0 +1,201 @@
+/*
+ * df.h — C ABI of the dual-flow Transformer decode library (libdf.so).
+ *
+ * The library runs the grouped dual-flow decode step on one GPU: the primary
+ * flow (a standard causal Transformer that owns the only KV cache) and the
+ * auxiliary flow (own token embedding, one-way coupling vectors a, b, c,
+ * read-only on the primary cache) are stacked into one pass, so every weight
+ * matrix and every KV region is read from HBM once per step for both flows.
+ * Source: "Resumen Técnico: Dual-Flow Transformers" (gist.science technical
+ * summary of arXiv 2608.12385), sections "Arquitectura Central",
+ * "Mecanismos Clave" and "Costes de Inferencia vs. Entrenamiento".
+ *
+ * Conventions for every entry point
+ *  - All pointers named "device" are CUDA device addresses owned by the
+ *    caller; the library borrows them and never frees them.  They must stay
+ *    valid until df_destroy.  "host" pointers are read or written before the
+ *    call returns (df_decode_step_host) or copied during df_create.
+ *  - Every call is asynchronous on the CUDA stream given to df_create unless
+ *    stated otherwise.  Argument, capacity and state errors are detected on
+ *    the host before anything is enqueued and leave the context unchanged.
+ *  - Errors detected on the device (a bounded wait that ran out, an index out
+ *    of range) are latched in a device word and reported by df_sync or by
+ *    the next call.  No call exits or aborts the process.
+ *  - df_last_error returns a NUL-terminated description of the last failure
+ *    (owned by the context, valid until the next call on it).
+ *
+ * Matrices are row-major [rows][cols] (PyTorch nn.Linear layout: out x in).
+ * Element type of matrices, embeddings and the KV cache is cfg.dtype (fp32
+ * or bf16); norm gains and coupling vectors are always fp32.
+ */
+#ifndef DF_H
+#define DF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DF_OK = 0,
+  DF_ERR_ARG = 1,          /* null pointer, bad size, unsupported combination      */
+  DF_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed                   */
+  DF_ERR_CAPACITY = 3,     /* batch > max_batch or position >= max_len            */
+  DF_ERR_STATE = 4,        /* decode before prefill, etc.                         */
+  DF_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (device error word)   */
+  DF_ERR_UNSUPPORTED = 6,  /* shape the kernels do not implement                  */
+  DF_ERR_DEVICE = 7        /* device-side bounds check failed (token id, expert)  */
+} df_status;
+
+typedef enum { DF_F32 = 0, DF_BF16 = 1 } df_dtype;
+
+/* Model shape and capacity.  n_experts == 0 selects the dense SwiGLU MLP of
+ * width ffn_hidden; n_experts > 0 selects the MoE MLP with top_k experts of
+ * width expert_hidden ("Mecanismos Clave", Replay de Router). */
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_hidden, vocab;
+  int n_experts, top_k, expert_hidden;
+  float rope_theta, norm_eps;
+  int dtype;               /* df_dtype */
+  int max_batch, max_len;  /* capacity of the KV cache and workspace        */
+} df_config;
+
+/* Parameter set (all device pointers; the struct and its per-layer arrays
+ * are host memory copied by df_create).  Both flows share every matrix
+ * except the token embeddings ("Arquitectura Central", Compartición de Pesos
+ * and Separación).
+ *
+ *  emb1, emb2   [vocab][d]                primary / auxiliary token embeddings
+ *  final_norm   [d] fp32                  final RMSNorm gain (shared)
+ *  lm_head      [vocab][d]                output matrix (shared, untied)
+ *  attn_norm[l] [d] fp32
+ *  wqkv[l]      [(Hq + 2*Hkv)*hd][d]      rows: Wq, then Wk, then Wv
+ *  wo[l]        [d][Hq*hd]
+ *  mlp_norm[l]  [d] fp32
+ *  wgu[l]       dense: [2F][d]; MoE: [E][2Fe][d].  Gate and up rows are
+ *               interleaved in blocks of 64: rows 128j..128j+63 are gate rows
+ *               64j..64j+63 and rows 128j+64..128j+127 the matching up rows.
+ *  wd[l]        dense: [d][F]; MoE: [E][d][Fe]
+ *  router[l]    MoE: [E][d]; NULL for dense models
+ *  a[l]         [Hq*hd] fp32   query coupling:        Q2 = Wq·u2 + a ⊙ q1 (pre-RoPE)
+ *  b[l]         [F or Fe] fp32 MLP-intermediate coupling: z2 += b ⊙ z1
+ *  c[l]         [d] fp32       MLP-output coupling:   y2 += c ⊙ y1
+ */
+typedef struct {
+  const void* emb1;
+  const void* emb2;
+  const float* final_norm;
+  const void* lm_head;
+  const float* const* attn_norm;
+  const void* const* wqkv;
+  const void* const* wo;
+  const float* const* mlp_norm;
+  const void* const* wgu;
+  const void* const* wd;
+  const void* const* router;
+  const float* const* a;
+  const float* const* b;
+  const float* const* c;
+} df_weights;
+
+typedef struct df_ctx df_ctx;
+
+/* Sizes of the two device buffers the caller allocates for a configuration:
+ * returns the workspace size in bytes and stores the KV-cache size in
+ * *kv_bytes (if non-NULL).  Returns 0 for an invalid configuration.
+ *
+ * KV-cache layout (primary flow only; the auxiliary flow never writes it):
+ *   [n_layers][2 (K, V)][max_batch][n_kv_heads][max_len][head_dim] of dtype,
+ * K stored after RoPE.  Positions 0..t-1 of sequence b are valid after
+ * prefill or decode has reached position t. */
+size_t df_workspace_bytes(const df_config* cfg, size_t* kv_bytes);
+
+/* Create a context.  kv_buf and workspace are device buffers of the sizes
+ * df_workspace_bytes reported (256-byte aligned); cuda_stream is a
+ * cudaStream_t (NULL = legacy default stream).  Builds TMA descriptors and
+ * launch plans; enqueues only memsets. */
+df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, void* workspace,
+                    void* cuda_stream, df_ctx** out);
+
+/* Prefill: run the primary flow alone over positions 0..n-1 of B sequences
+ * and write their K/V ("Arquitectura Central": the auxiliary flow is
+ * skipped during prefill).  tokens: device int32 [B][n].  Resets the
+ * position to n.  For a prompt of length P the caller prefills P-1 tokens
+ * and passes the last prompt token to the first df_decode_step, where the
+ * auxiliary flow is active.  n may be 0 (empty prompt). */
+df_status df_prefill(df_ctx* ctx, const int32_t* tokens, int B, int n);
+
+/* Declare that the caller has written positions 0..t-1 of B sequences into
+ * the KV cache itself (restoring a saved cache).  Next decode runs at t. */
+df_status df_set_length(df_ctx* ctx, int B, int t);
+
+/* One grouped decode step at position t for the B sequences of the last
+ * prefill: both flows, K/V appended at t for the primary flow only, then the
+ * mixture p_mix = alpha*p1 + (1-alpha)*p2 with alpha = 0.5 + 0.5*sum(p1^2)
+ * ("Mecanismos Clave", Objetivo de Mezcla).  tokens: device int32 [B].
+ * Outputs (device, each may be NULL): logp_mix fp32 [B][vocab],
+ * argmax int32 [B] (lowest index among equal maxima), alpha fp32 [B].
+ * Advances the position to t+1.  DF_ERR_CAPACITY if t >= max_len. */
+df_status df_decode_step(df_ctx* ctx, const int32_t* tokens, float* logp_mix, int32_t* argmax,
+                         float* alpha);
+
+/* The same step with HOST buffers: copies tokens (host int32 [B]) to the
+ * device, runs the step, copies the outputs back (host, each may be NULL)
+ * and synchronises the stream before returning.  Pinned host memory gives
+ * asynchronous copies; pageable memory works but is slower. */
+df_status df_decode_step_host(df_ctx* ctx, const int32_t* tokens, float* logp_mix,
+                              int32_t* argmax, float* alpha);
+
+/* Execution mode for later decode steps.
+ *  aux_on = 0: standard decode (primary flow only); logp_mix receives
+ *              log p1, alpha receives 1.
+ *  ungrouped = 1: the ablation that runs the primary flow and then the
+ *              auxiliary flow as two passes, re-reading every weight and KV
+ *              region; results are identical to the grouped step. */
+df_status df_set_mode(df_ctx* ctx, int aux_on, int ungrouped);
+
+/* Optional per-step diagnostics written by later decode steps (device
+ * pointers, each may be NULL): logp1, logp2 fp32 [B][vocab]; topk int32
+ * [n_layers][B][top_k] (MoE primary expert indices, descending router
+ * logit); router fp32 [n_layers][B][n_experts] (primary router logits). */
+df_status df_debug_outputs(df_ctx* ctx, float* logp1, float* logp2, int32_t* topk, float* router);
+
+/* Synchronise the stream and report any latched device error. */
+df_status df_sync(df_ctx* ctx);
+
+/* Current position (number of valid cache positions). */
+int df_length(const df_ctx* ctx);
+
+/* Number of kernels in the last captured step graph (decode or prefill
+ * position), or -1 when steps run without graph capture. */
+int df_step_kernels(const df_ctx* ctx);
+
+/* Bench hook: re-run one operation of the step `iters` times on the
+ * context's stream, cycling through the layers (so consecutive launches read
+ * different weights and no launch is served from L2 by its predecessor),
+ * bracketed by CUDA events; *avg_ms receives the mean time per launch.
+ * Operations re-execute on the current buffers and are idempotent for the
+ * cache contents of valid positions.  Needs a previous decode step. */
+enum {
+  DF_OP_QKV = 0,     /* fused QKV projection + coupling + RoPE + cache append */
+  DF_OP_ATTN = 1,    /* shared-KV split attention + split merge               */
+  DF_OP_WO = 2,      /* output projection + residual                         */
+  DF_OP_GATEUP = 3,  /* gate/up projection + SwiGLU + b coupling (dense)     */
+  DF_OP_DOWN = 4,    /* down projection + c coupling + residual (dense)      */
+  DF_OP_LMHEAD = 5,  /* LM head                                              */
+  DF_OP_MOE = 6      /* router + replayed experts + combine (MoE)            */
+};
+df_status df_time_op(df_ctx* ctx, int op, int iters, float* avg_ms);
+
+const char* df_last_error(const df_ctx* ctx);
+
+/* Release host state (graphs, plans).  Device buffers stay with the caller. */
+void df_destroy(df_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DF_H */

@@ -1,0 +1,155 @@
+"""Shared helpers of the GPU-vs-oracle parity tests."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import dfsynth
+from dfsynth.gen import Weights
+from oracle import Oracle
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def tied_weights(cfg, seed=0, a=0.0, b=0.0, c=0.0):
+    w = Weights(cfg, seed)
+    ov = {("emb2",): w[("emb1",)]}
+    for l in range(cfg.n_layers):
+        ov[(l, "a")] = np.full(cfg.q_dim, a, np.float32)
+        ov[(l, "b")] = np.full(cfg.mlp_hidden, b, np.float32)
+        ov[(l, "c")] = np.full(cfg.d_model, c, np.float32)
+    return Weights(cfg, seed, overrides=ov)
+
+
+class GpuRun:
+    """Runs prefill + teacher-forced decode steps through the C-ABI and keeps
+    every step's outputs on the host."""
+
+    def __init__(self, cfg, weights, tok, aux=True, ungrouped=False, steps=None, debug=True, max_len=None):
+        import torch
+        from dual_flow_transformer_decode_b300.model import DualFlowModel
+        self.cfg = cfg
+        B = tok.shape[0]
+        dev = torch.device("cuda")
+        self.m = DualFlowModel(cfg, weights, max_batch=B, max_len=max_len or cfg.max_len)
+        self.m.set_mode(aux, ungrouped)
+        V = cfg.vocab
+        lp = torch.zeros(B, V, device=dev)
+        am = torch.zeros(B, dtype=torch.int32, device=dev)
+        al = torch.zeros(B, device=dev)
+        l1 = torch.zeros(B, V, device=dev)
+        l2 = torch.zeros(B, V, device=dev)
+        tk = torch.zeros(cfg.n_layers, B, max(cfg.top_k, 1), dtype=torch.int32, device=dev)
+        rl = torch.zeros(cfg.n_layers, B, max(cfg.n_experts, 1), device=dev)
+        if debug:
+            self.m.debug_outputs(l1, l2 if aux else None, tk if cfg.n_experts else None,
+                                 rl if cfg.n_experts else None)
+        tok_d = torch.from_numpy(np.ascontiguousarray(tok)).to(dev)
+        self.m.prefill(tok_d[:, :cfg.n_prefill].contiguous())
+        self.steps = []
+        step_tok = torch.zeros(B, dtype=torch.int32, device=dev)
+        for s in range(steps if steps is not None else cfg.n_steps):
+            step_tok.copy_(tok_d[:, cfg.n_prefill + s])
+            self.m.decode_step(step_tok, lp, am, al)
+            self.m.sync()
+            r = {"logp_mix": lp.double().cpu().numpy(), "argmax": am.cpu().numpy().astype(np.int64),
+                 "alpha": al.double().cpu().numpy(), "logp1": l1.double().cpu().numpy()}
+            if aux:
+                r["logp2"] = l2.double().cpu().numpy()
+            if cfg.n_experts:
+                r["topk"] = tk.cpu().numpy().astype(np.int64)
+                r["router1"] = rl.double().cpu().numpy()
+            self.steps.append(r)
+        self.kv = self.m.kv_view().float().cpu().numpy()
+
+    def close(self):
+        self.m.close()
+
+
+def oracle_run(cfg, weights, tok, steps=None, aux=True):
+    o = Oracle(cfg, weights, tok.shape[0])
+    o.prefill(tok[:, :cfg.n_prefill])
+    outs = [o.decode_step(tok[:, cfg.n_prefill + s], aux=aux) for s in range(steps if steps is not None else cfg.n_steps)]
+    return o, outs
+
+
+def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
+    """Element-wise comparison; returns a report dict.  seq_map maps oracle
+    sequence index -> GPU batch index.
+
+    Integer decisions: with eps = max |GPU - oracle| over the values a
+    decision ranks (one row of log p_mix, or one row of router logits), two
+    entries whose oracle values differ by more than 2*eps cannot change order.
+    Such decisions must match exactly.  A decision whose margin is at most
+    2*eps is a near tie: the GPU's choice must then be a valid one, i.e. its
+    oracle value within 2*eps of the oracle's choice.
+    """
+    tol = TOL[cfg.dtype]
+    rep = {"max_dlogp_mix": 0.0, "max_dlogp1": 0.0, "max_dalpha": 0.0, "argmax_mismatch": [],
+           "near_ties": [], "invalid_near_ties": [], "topk_mismatch": [], "max_drouter": 0.0,
+           "decisions": 0}
+    for s, (g, o) in enumerate(zip(gpu_steps, ora_steps)):
+        nb = o["logp1"].shape[0]
+        idx = list(range(nb)) if seq_map is None else seq_map
+        d1 = np.abs(g["logp1"][idx] - o["logp1"]).max()
+        rep["max_dlogp1"] = max(rep["max_dlogp1"], float(d1))
+        if "logp_mix" in o:
+            dmix = np.abs(g["logp_mix"][idx] - o["logp_mix"])
+            rep["max_dlogp_mix"] = max(rep["max_dlogp_mix"], float(dmix.max()))
+            rep["max_dalpha"] = max(rep["max_dalpha"], float(np.abs(g["alpha"][idx] - o["alpha"]).max()))
+            for i, b in enumerate(idx):
+                eps = float(dmix[i].max())
+                rep["decisions"] += 1
+                ga, oa = int(g["argmax"][b]), int(o["argmax"][i])
+                if o["argmax_margin"][i] <= 2 * eps:
+                    rep["near_ties"].append(("argmax", s, i, float(o["argmax_margin"][i]), eps))
+                    if o["logp_mix"][i][oa] - o["logp_mix"][i][ga] > 2 * eps:
+                        rep["invalid_near_ties"].append(("argmax", s, i, ga, oa))
+                elif ga != oa:
+                    rep["argmax_mismatch"].append((s, i, ga, oa, float(o["argmax_margin"][i]), eps))
+        if cfg.n_experts:
+            dr = np.abs(g["router1"][:, idx] - o["router1"])
+            rep["max_drouter"] = max(rep["max_drouter"], float(dr.max()))
+            for l in range(cfg.n_layers):
+                for i, b in enumerate(idx):
+                    eps = float(dr[l, i].max())
+                    rep["decisions"] += 1
+                    gs, os_ = g["topk"][l, b], o["topk"][l, i]
+                    if o["topk_margin"][l, i] <= 2 * eps:
+                        rep["near_ties"].append(("topk", s, l, i, float(o["topk_margin"][l, i]), eps))
+                        r = o["router1"][l][i]
+                        if r[os_].min() - r[gs].min() > 2 * eps:
+                            rep["invalid_near_ties"].append(("topk", s, l, i, gs.tolist(), os_.tolist()))
+                    elif set(gs.tolist()) != set(os_.tolist()):
+                        rep["topk_mismatch"].append((s, l, i, gs.tolist(), os_.tolist(),
+                                                     float(o["topk_margin"][l, i]), eps))
+    rep["tol"] = tol
+    return rep
+
+
+def assert_parity(cfg, rep, max_near_tie_frac=0.25):
+    tol = rep["tol"]
+    assert rep["max_dlogp_mix"] <= tol, rep
+    assert rep["max_dlogp1"] <= tol, rep
+    assert not rep["argmax_mismatch"], rep["argmax_mismatch"][:5]
+    assert not rep["topk_mismatch"], rep["topk_mismatch"][:5]
+    assert not rep["invalid_near_ties"], rep["invalid_near_ties"][:5]
+    # near ties are allowed but must stay a minority of the compared decisions
+    assert len(rep["near_ties"]) <= max_near_tie_frac * max(rep["decisions"], 1), rep["near_ties"][:5]
+
+
+def kv_compare(cfg, gpu_kv, oracle, n_pos, seqs_gpu, seqs_or=None):
+    """Max |difference| and fraction of exactly equal elements between the GPU
+    cache and the oracle's cache over positions 0..n_pos-1."""
+    seqs_or = seqs_or if seqs_or is not None else list(range(len(seqs_gpu)))
+    mx, eq, tot = 0.0, 0, 0
+    for l in range(cfg.n_layers):
+        for i, b in zip(seqs_or, seqs_gpu):
+            for kind, arr in ((0, oracle.K), (1, oracle.V)):
+                g = gpu_kv[l, kind, b, :, :n_pos].astype(np.float64)
+                o = arr[l][i][:, :n_pos]
+                d = np.abs(g - o)
+                mx = max(mx, float(d.max()))
+                eq += int((d == 0).sum())
+                tot += d.size
+    return mx, eq / max(tot, 1)

@@ -1,0 +1,59 @@
+"""CPU checks of the C-ABI library: it loads, exports every entry point that
+include/df.h declares, and sizes buffers on the host."""
+
+import os
+import re
+
+import pytest
+
+import dfsynth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(df_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dual_flow_transformer_decode_b300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = _declared()
+    assert "df_decode_step" in decl and "df_create" in decl
+    for n in decl:
+        assert hasattr(lib, n), n
+    from dual_flow_transformer_decode_b300 import binding
+    assert sorted(binding.EXPORTS) == sorted(decl)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "dense1b_ctx1k", "dense1b_ctx32k", "dense24l_b128", "moe64e_top4"])
+def test_workspace_sizes(lib, name):
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config(name)
+    ws, kv = binding.df_workspace_bytes(binding.make_config(cfg, cfg.batch, cfg.max_len))
+    assert ws > 0
+    esz = 2 if cfg.dtype == "bf16" else 4
+    assert kv == cfg.n_layers * 2 * cfg.batch * cfg.n_kv_heads * cfg.max_len * cfg.head_dim * esz
+
+
+def test_invalid_configs_rejected(lib):
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config("tiny_fp32")
+    good = binding.make_config(cfg, 1, 16)
+    assert binding.df_workspace_bytes(good)[0] > 0
+    for field, val in [("n_heads", 3), ("head_dim", 31), ("ffn_hidden", 100), ("max_batch", 0),
+                       ("dtype", 5), ("vocab", 0)]:
+        c = binding.make_config(cfg, 1, 16)
+        setattr(c, field, val)
+        assert binding.df_workspace_bytes(c)[0] == 0, field
