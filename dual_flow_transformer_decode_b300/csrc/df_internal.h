@@ -5,9 +5,32 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace df {
+
+// Programmatic dependent launch (on unless DF_NO_PDL=1): a kernel may start
+// while its predecessor drains; every kernel calls griddepcontrol.wait before
+// it touches the predecessor's outputs.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
 
 // Model dimensions plus derived sizes, fixed at df_create.
 struct Dims {
@@ -17,6 +40,7 @@ struct Dims {
   int maxB, max_len;
   int qdim, kvdim, qkvn, G, Fm;   // Fm = MLP hidden of one expert or of the dense MLP
   int esz;         // element size of dtype
+  int sms;         // streaming multiprocessors of the device
 };
 
 // Device buffers carved out of the caller's workspace.
@@ -50,6 +74,7 @@ struct Buffers {
   float* out_alpha; // [maxB]
   float* rope;      // [max_len][hd/2][2] cos, sin
   int* tickets;     // split-K tile tickets
+  int* attn_tickets;  // [maxB][Hkv] split-merge tickets of the attention kernel
   size_t tickets_cap;
   float* gpart;     // split-K partial tiles
   size_t gpart_cap; // floats

@@ -106,6 +106,7 @@ bool valid_config(const df_config* c, std::string* why) {
     return bad("non-positive model size");
   if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
   if (c->head_dim % 2) return bad("head_dim must be even (RoPE pairs)");
+  if (c->d_model % 8 || c->d_model > 8192) return bad("d_model must be a multiple of 8 and at most 8192");
   if (c->dtype != DF_F32 && c->dtype != DF_BF16) return bad("dtype must be DF_F32 or DF_BF16");
   if (c->max_batch <= 0 || c->max_len <= 0) return bad("max_batch and max_len must be positive");
   if (c->max_batch > 4096) return bad("max_batch above 4096");
@@ -143,6 +144,11 @@ Dims make_dims(const df_config* c) {
   D.G = D.Hq / D.Hkv;
   D.Fm = D.E ? D.Fe : D.F;
   D.esz = D.bf16 ? 2 : 4;
+  // the split plan and workspace size depend on the SM count of the current device
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  D.sms = sms;
   return D;
 }
 
@@ -197,6 +203,7 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.rope = (float*)take((size_t)D.max_len * D.hd * 4);
   b.tickets_cap = df::tc_tickets_needed(D);
   b.tickets = (int*)take(b.tickets_cap * 4);
+  b.attn_tickets = (int*)take((size_t)D.maxB * D.Hkv * 4);
   b.gpart_cap = df::tc_partial_floats(D);
   b.gpart = (float*)take(b.gpart_cap * 4);
   if (Bf) *Bf = b;
@@ -239,11 +246,11 @@ void op_qkv(df_ctx* X, int l, const Rows& R, const Couple& C) {
 void op_attn(df_ctx* X, int l, const Rows& R) {
   const Dims& D = X->D;
   if (!X->force_generic && df::attn_fast_can_run(X->at, D)) {
-    df::attn_fast(X->at, D, X->Bf, X->kv, l, X->splits, R, X->stream);
+    df::attn_fast(X->at, D, X->Bf, X->kv, l, X->splits, R, X->stream);  // merges its splits itself
   } else {
     df::launch_attention_generic(D, X->Bf, X->kv, l, X->splits, R, X->stream);
+    df::launch_attn_combine(D, X->Bf, X->splits, R, X->stream);
   }
-  df::launch_attn_combine(D, X->Bf, X->splits, R, X->stream);
 }
 
 // Output projection + residual.
@@ -251,7 +258,7 @@ void op_wo(df_ctx* X, int l, const Rows& R) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::RESID)) {
-    df::tc_resid(X->tc, D, Bf, X->wo[l], R, X->stream);
+    df::tc_resid(X->tc, D, Bf, X->wo[l], l, R, X->stream);
   } else {
     df::launch_gemv(D, X->wo[l], D.d, D.qdim, Bf.o, D.qdim, 0, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_residual(D, Bf, Bf.raw, Bf.rawN, R, X->stream);
@@ -263,7 +270,7 @@ void op_gateup(df_ctx* X, int l, const Rows& R, const Couple& C) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::SWIGLU)) {
-    df::tc_swiglu(X->tc, D, Bf, X->wgu[l], X->b[l], C, R, X->stream);
+    df::tc_swiglu(X->tc, D, Bf, X->wgu[l], l, X->b[l], C, R, X->stream);
   } else {
     df::launch_gemv(D, X->wgu[l], 2 * D.F, D.d, Bf.u, D.d, 0, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_swiglu(D, Bf, Bf.raw, Bf.rawN, X->b[l], C, R, X->stream);
@@ -275,7 +282,7 @@ void op_down(df_ctx* X, int l, const Rows& R, const Couple& C) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::DOWN)) {
-    df::tc_down(X->tc, D, Bf, X->wd[l], X->c[l], C, R, X->stream);
+    df::tc_down(X->tc, D, Bf, X->wd[l], l, X->c[l], C, R, X->stream);
   } else {
     df::launch_gemv(D, X->wd[l], D.d, D.F, Bf.z, D.F, 0, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_down(D, Bf, Bf.raw, Bf.rawN, X->c[l], C, R, X->stream);

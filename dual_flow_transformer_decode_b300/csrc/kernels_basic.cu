@@ -9,15 +9,27 @@
 // 0..B-1 primary flow, B..2B-1 auxiliary flow (same sequence order).
 
 #include <math.h>
+#include <stdlib.h>
+
+#include <cmath>
 
 #include "df_internal.h"
+#include "ptx.cuh"
 
 namespace df {
 
 // ------------------------------------------------------------------ position
 
-__global__ void k_set_pos(Ctrl* c, int t) { c->t = t; }
-__global__ void k_advance_pos(Ctrl* c) { c->t += 1; }
+__global__ void k_set_pos(Ctrl* c, int t) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  c->t = t;
+}
+__global__ void k_advance_pos(Ctrl* c) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  c->t += 1;
+}
 
 template <typename T>
 __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
@@ -25,13 +37,22 @@ __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restric
                                float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
                                int splits, int flo, int fhi);
 
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("DF_NO_PDL");
+    v = (e && e[0] == '1') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 void kernels_init() {
   cudaFuncSetAttribute(k_attn_generic<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   cudaFuncSetAttribute(k_attn_generic<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
-void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { k_set_pos<<<1, 1, 0, s>>>(c, t); }
-void launch_advance_pos(Ctrl* c, cudaStream_t s) { k_advance_pos<<<1, 1, 0, s>>>(c); }
+void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { launch_pdl(k_set_pos, dim3(1), dim3(1), 0, s, c, t); }
+void launch_advance_pos(Ctrl* c, cudaStream_t s) { launch_pdl(k_advance_pos, dim3(1), dim3(1), 0, s, c); }
 
 // ------------------------------------------------------------------ embedding
 // h[b] = E1[x_b], h[B+b] = E2[x_b]: the two flows use separate token
@@ -41,6 +62,8 @@ template <typename T>
 __global__ void k_embed(const T* __restrict__ e1, const T* __restrict__ e2, const int32_t* __restrict__ tok,
                         int tok_stride, int use_pos, Ctrl* ctrl, float* __restrict__ h, int B, int lo, int d,
                         int V) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
   int idx = b * tok_stride + (use_pos ? ctrl->t : 0);
@@ -57,10 +80,10 @@ void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void
   int n = R.hi - R.lo;
   if (n <= 0) return;
   if (D.bf16)
-    k_embed<__nv_bfloat16><<<n, 256, 0, s>>>((const __nv_bfloat16*)emb1, (const __nv_bfloat16*)emb2, tokens,
+    launch_pdl(k_embed<__nv_bfloat16>, dim3(n), dim3(256), 0, s, (const __nv_bfloat16*)emb1, (const __nv_bfloat16*)emb2, tokens,
                                               tok_stride, use_pos, Bf.ctrl, Bf.h, R.B, R.lo, D.d, D.V);
   else
-    k_embed<float><<<n, 256, 0, s>>>((const float*)emb1, (const float*)emb2, tokens, tok_stride, use_pos,
+    launch_pdl(k_embed<float>, dim3(n), dim3(256), 0, s, (const float*)emb1, (const float*)emb2, tokens, tok_stride, use_pos,
                                      Bf.ctrl, Bf.h, R.B, R.lo, D.d, D.V);
 }
 
@@ -69,19 +92,51 @@ void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void
 // next GEMM; optionally also kept unrounded in fp32 (MoE router input).
 
 template <typename T>
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a, float b, float c, float d) {
+  __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(p);
+  q[0] = __floats2bfloat162_rn(a, b);
+  q[1] = __floats2bfloat162_rn(c, d);
+}
+
+// One CTA (256 threads) per row; the row is held in registers as float4
+// (d <= 8192, d a multiple of 4), so it is read once.
+template <typename T>
 __global__ void k_rmsnorm(const float* __restrict__ h, const float* __restrict__ g, T* __restrict__ out,
                           float* __restrict__ out_f32, int d, float eps, int lo) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   __shared__ float red[32];
-  int m = lo + blockIdx.x;
-  const float* x = h + (size_t)m * d;
+  const int m = lo + blockIdx.x;
+  const float4* x4 = reinterpret_cast<const float4*>(h + (size_t)m * d);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  const int n4 = d >> 2;
+  float4 v[8];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) ss += x[i] * x[i];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = threadIdx.x + k * 256;
+    if (i < n4) {
+      v[k] = x4[i];
+      ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+  }
   ss = block_sum(ss, red);
-  float r = 1.0f / sqrtf(ss / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = x[i] * r * g[i];
-    out[(size_t)m * d + i] = Num<T>::from_f(v);
-    if (out_f32) out_f32[(size_t)m * d + i] = v;
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = threadIdx.x + k * 256;
+    if (i < n4) {
+      const float4 gg = g4[i];
+      const float a = v[k].x * r * gg.x, b = v[k].y * r * gg.y, c = v[k].z * r * gg.z, e = v[k].w * r * gg.w;
+      store4<T>(out + (size_t)m * d + 4 * i, a, b, c, e);
+      if (out_f32) *reinterpret_cast<float4*>(out_f32 + (size_t)m * d + 4 * i) = make_float4(a, b, c, e);
+    }
   }
 }
 
@@ -90,9 +145,9 @@ void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out,
   int n = R.hi - R.lo;
   if (n <= 0) return;
   if (D.bf16)
-    k_rmsnorm<__nv_bfloat16><<<n, 256, 0, s>>>(Bf.h, g, (__nv_bfloat16*)out, out_f32, D.d, D.eps, R.lo);
+    launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(n), dim3(256), 0, s, Bf.h, g, (__nv_bfloat16*)out, out_f32, D.d, D.eps, R.lo);
   else
-    k_rmsnorm<float><<<n, 256, 0, s>>>(Bf.h, g, (float*)out, out_f32, D.d, D.eps, R.lo);
+    launch_pdl(k_rmsnorm<float>, dim3(n), dim3(256), 0, s, Bf.h, g, (float*)out, out_f32, D.d, D.eps, R.lo);
 }
 
 // ------------------------------------------------------------------ GEMV (CUDA cores)
@@ -104,6 +159,8 @@ void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out,
 template <typename TW, typename TX, int R>
 __global__ void k_gemv(const TW* __restrict__ W, int N, int K, const TX* __restrict__ X, int ldx,
                        float* __restrict__ out, int ldo, int lo, int hi) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int n = blockIdx.x * warps + w; n < N; n += gridDim.x * warps) {
     const TW* wr = W + (size_t)n * K;
@@ -133,13 +190,13 @@ void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int 
   if (blocks > 148 * 16) blocks = 148 * 16;
   if (D.bf16) {
     if (x_f32)
-      k_gemv<__nv_bfloat16, float, 8><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)W, N, K, (const float*)X, ldx,
+      launch_pdl(k_gemv<__nv_bfloat16, float, 8>, dim3(blocks), dim3(256), 0, s, (const __nv_bfloat16*)W, N, K, (const float*)X, ldx,
                                                               out, ldo, R.lo, R.hi);
     else
-      k_gemv<__nv_bfloat16, __nv_bfloat16, 8><<<blocks, 256, 0, s>>>(
+      launch_pdl(k_gemv<__nv_bfloat16, __nv_bfloat16, 8>, dim3(blocks), dim3(256), 0, s, 
           (const __nv_bfloat16*)W, N, K, (const __nv_bfloat16*)X, ldx, out, ldo, R.lo, R.hi);
   } else {
-    k_gemv<float, float, 8><<<blocks, 256, 0, s>>>((const float*)W, N, K, (const float*)X, ldx, out, ldo, R.lo,
+    launch_pdl(k_gemv<float, float, 8>, dim3(blocks), dim3(256), 0, s, (const float*)W, N, K, (const float*)X, ldx, out, ldo, R.lo,
                                                    R.hi);
   }
 }
@@ -157,6 +214,8 @@ template <typename T>
 __global__ void k_ep_qkv(const float* __restrict__ raw, int ldr, const float* __restrict__ a, T* __restrict__ kvl,
                          const float* __restrict__ rope, const Ctrl* __restrict__ ctrl, float* __restrict__ qatt,
                          Couple C, int B, int lo, int Hq, int Hkv, int hd, int maxB, int max_len) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
   int t = ctrl->t;
@@ -208,11 +267,11 @@ void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, 
   if (n <= 0) return;
   size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
   if (D.bf16)
-    k_ep_qkv<__nv_bfloat16><<<n, 256, 0, s>>>(raw, ldr, a, (__nv_bfloat16*)kv + layer * layer_elems, Bf.rope,
+    launch_pdl(k_ep_qkv<__nv_bfloat16>, dim3(n), dim3(256), 0, s, raw, ldr, a, (__nv_bfloat16*)kv + layer * layer_elems, Bf.rope,
                                                Bf.ctrl, Bf.qatt, C, R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB,
                                                D.max_len);
   else
-    k_ep_qkv<float><<<n, 256, 0, s>>>(raw, ldr, a, (float*)kv + layer * layer_elems, Bf.rope, Bf.ctrl, Bf.qatt, C,
+    launch_pdl(k_ep_qkv<float>, dim3(n), dim3(256), 0, s, raw, ldr, a, (float*)kv + layer * layer_elems, Bf.rope, Bf.ctrl, Bf.qatt, C,
                                       R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB, D.max_len);
 }
 
@@ -222,6 +281,8 @@ void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, 
 template <typename T>
 __global__ void k_ep_swiglu(const float* __restrict__ raw, int ldr, const float* __restrict__ bvec,
                             T* __restrict__ z, Couple C, int B, int lo, int F) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
   for (int fi = threadIdx.x; fi < F; fi += blockDim.x) {
@@ -243,15 +304,17 @@ void launch_ep_swiglu(const Dims& D, const Buffers& Bf, const float* raw, int ld
   int n = R.hi - R.lo;
   if (n <= 0) return;
   if (D.bf16)
-    k_ep_swiglu<__nv_bfloat16><<<n, 256, 0, s>>>(raw, ldr, bvec, (__nv_bfloat16*)Bf.z, C, R.B, R.lo, D.F);
+    launch_pdl(k_ep_swiglu<__nv_bfloat16>, dim3(n), dim3(256), 0, s, raw, ldr, bvec, (__nv_bfloat16*)Bf.z, C, R.B, R.lo, D.F);
   else
-    k_ep_swiglu<float><<<n, 256, 0, s>>>(raw, ldr, bvec, (float*)Bf.z, C, R.B, R.lo, D.F);
+    launch_pdl(k_ep_swiglu<float>, dim3(n), dim3(256), 0, s, raw, ldr, bvec, (float*)Bf.z, C, R.B, R.lo, D.F);
 }
 
 // Down-projection epilogue with the MLP-output coupling: y2 += c ⊙ y1, then
 // the residual add h += y for both flows.
 __global__ void k_ep_down(const float* __restrict__ raw, int ldr, const float* __restrict__ cvec,
                           float* __restrict__ h, Couple C, int B, int lo, int d) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
@@ -270,10 +333,12 @@ void launch_ep_down(const Dims& D, const Buffers& Bf, const float* raw, int ldr,
                     const Couple& C, const Rows& R, cudaStream_t s) {
   int n = R.hi - R.lo;
   if (n <= 0) return;
-  k_ep_down<<<n, 256, 0, s>>>(raw, ldr, cvec, Bf.h, C, R.B, R.lo, D.d);
+  launch_pdl(k_ep_down, dim3(n), dim3(256), 0, s, raw, ldr, cvec, Bf.h, C, R.B, R.lo, D.d);
 }
 
 __global__ void k_ep_residual(const float* __restrict__ raw, int ldr, float* __restrict__ h, int lo, int d) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   for (int n = threadIdx.x; n < d; n += blockDim.x) h[(size_t)m * d + n] += raw[(size_t)m * ldr + n];
 }
@@ -282,7 +347,7 @@ void launch_ep_residual(const Dims& D, const Buffers& Bf, const float* raw, int 
                         cudaStream_t s) {
   int n = R.hi - R.lo;
   if (n <= 0) return;
-  k_ep_residual<<<n, 256, 0, s>>>(raw, ldr, Bf.h, R.lo, D.d);
+  launch_pdl(k_ep_residual, dim3(n), dim3(256), 0, s, raw, ldr, Bf.h, R.lo, D.d);
 }
 
 // ------------------------------------------------------------------ attention
@@ -293,13 +358,26 @@ void launch_ep_residual(const Dims& D, const Buffers& Bf, const float* raw, int 
 // unnormalised output o per query row; attn_combine merges the splits.
 // Partial slot of a query row: ((b*Hkv + g)*splits + s)*2G + f*G + j.
 
+// Splits per (sequence, KV head): the count whose CTAs fill the GPU's
+// resident slots (2 per SM) with the least wave-quantisation loss, keeping
+// at least 4 tiles of 64 positions per split at full length.
 int attn_splits(const Dims& D, int B) {
-  int pairs = B * D.Hkv;
-  int want = (2 * 148 + pairs - 1) / pairs;
-  int maxs = (D.max_len + 63) / 64;
-  if (want > maxs) want = maxs;
-  if (want < 1) want = 1;
-  return want;
+  const int pairs = B * D.Hkv;
+  const int slots = 2 * D.sms;
+  int maxs = D.max_len / 256;
+  if (maxs < 1) maxs = 1;
+  if (maxs > 16) maxs = 16;  // the splits of a (sequence, KV head) form one thread-block cluster
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= maxs; ++s) {
+    double x = (double)pairs * s / slots;
+    double eff = x / std::ceil(x);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
 }
 
 __device__ __forceinline__ void split_range(int n, int splits, int s, int& s0, int& s1) {
@@ -314,6 +392,8 @@ __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restric
                                const Ctrl* __restrict__ ctrl, float* __restrict__ part_o,
                                float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
                                int splits, int flo, int fhi) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   constexpr int CH = 128;  // positions per chunk == blockDim.x
   extern __shared__ float sm[];
   int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -402,11 +482,11 @@ void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, 
   dim3 grid(splits, D.Hkv, R.B);
   size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
   if (D.bf16) {
-    k_attn_generic<__nv_bfloat16><<<grid, 128, smem, s>>>((const __nv_bfloat16*)kv + layer * layer_elems, Bf.qatt,
+    launch_pdl(k_attn_generic<__nv_bfloat16>, dim3(grid), dim3(128), smem, s, (const __nv_bfloat16*)kv + layer * layer_elems, Bf.qatt,
                                                           Bf.ctrl, Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd,
                                                           D.maxB, D.max_len, splits, flo, fhi);
   } else {
-    k_attn_generic<float><<<grid, 128, smem, s>>>((const float*)kv + layer * layer_elems, Bf.qatt, Bf.ctrl,
+    launch_pdl(k_attn_generic<float>, dim3(grid), dim3(128), smem, s, (const float*)kv + layer * layer_elems, Bf.qatt, Bf.ctrl,
                                                   Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd, D.maxB, D.max_len,
                                                   splits, flo, fhi);
   }
@@ -417,6 +497,8 @@ void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, 
 template <typename T>
 __global__ void k_attn_combine(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                T* __restrict__ out, int B, int Hkv, int G, int hd, int splits, int flo) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int b = blockIdx.x, head = blockIdx.y, f = flo + blockIdx.z;
   int g = head / G, j = head % G;
   int qdim = Hkv * G * hd;
@@ -444,10 +526,10 @@ void launch_attn_combine(const Dims& D, const Buffers& Bf, int splits, const Row
   int flo = R.lo >= R.B ? 1 : 0, fhi = R.hi > R.B ? 2 : 1;
   dim3 grid(R.B, D.Hq, fhi - flo);
   if (D.bf16)
-    k_attn_combine<__nv_bfloat16><<<grid, 128, 0, s>>>(Bf.part_o, Bf.part_ml, (__nv_bfloat16*)Bf.o, R.B, D.Hkv,
+    launch_pdl(k_attn_combine<__nv_bfloat16>, dim3(grid), dim3(128), 0, s, Bf.part_o, Bf.part_ml, (__nv_bfloat16*)Bf.o, R.B, D.Hkv,
                                                         D.G, D.hd, splits, flo);
   else
-    k_attn_combine<float><<<grid, 128, 0, s>>>(Bf.part_o, Bf.part_ml, (float*)Bf.o, R.B, D.Hkv, D.G, D.hd, splits,
+    launch_pdl(k_attn_combine<float>, dim3(grid), dim3(128), 0, s, Bf.part_o, Bf.part_ml, (float*)Bf.o, R.B, D.Hkv, D.G, D.hd, splits,
                                                flo);
 }
 
@@ -467,6 +549,8 @@ __device__ __forceinline__ float logaddexp_f(float x, float y) {
 __global__ void k_mix(const float* __restrict__ logits, int B, int V, int aux_on, float* __restrict__ logp_mix,
                       int32_t* __restrict__ argmax, float* __restrict__ alpha_out, float* __restrict__ logp1,
                       float* __restrict__ logp2) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   __shared__ float red[32];
   __shared__ float redv[32];
   __shared__ int redi[32];
@@ -551,7 +635,7 @@ __global__ void k_mix(const float* __restrict__ logits, int B, int V, int aux_on
 
 void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax, float* alpha,
                 float* logp1, float* logp2, cudaStream_t s) {
-  k_mix<<<B, 1024, 0, s>>>(Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
+  launch_pdl(k_mix, dim3(B), dim3(1024), 0, s, Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
 }
 
 // ------------------------------------------------------------------ MoE (router replay)
@@ -565,6 +649,8 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
                             int* __restrict__ ecount, int* __restrict__ elist, int B, int E, int k, int maxB,
                             int select, int prim, int aux, int32_t* __restrict__ dbg_topk_l,
                             float* __restrict__ dbg_router_l) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     if (select) {
       const float* r = rlog + (size_t)b * E;
@@ -609,7 +695,7 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
 void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
                       float* dbg_router, cudaStream_t s) {
   int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  k_moe_route<<<1, 256, 0, s>>>(Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, R.B, D.E, D.k, D.maxB, select,
+  launch_pdl(k_moe_route, dim3(1), dim3(256), 0, s, Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, R.B, D.E, D.k, D.maxB, select,
                                 R.has_primary(), R.has_aux(),
                                 dbg_topk ? dbg_topk + (size_t)layer * R.B * D.k : nullptr,
                                 dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);
@@ -621,6 +707,8 @@ template <typename T>
 __global__ void k_moe_gateup(const T* __restrict__ wgu, const float* __restrict__ bvec, const T* __restrict__ u,
                              const int* __restrict__ ecount, const int* __restrict__ elist, T* __restrict__ zE,
                              Couple C, int B, int d, int Fe, int k, int maxB, int prim, int aux) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int e = blockIdx.x;
   int cnt = ecount[e];
   if (cnt == 0) return;
@@ -661,11 +749,11 @@ void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu
                                const Couple& C, const Rows& R, cudaStream_t s) {
   dim3 grid(D.E, (D.Fe + 7) / 8);
   if (D.bf16)
-    k_moe_gateup<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)wgu, bvec, (const __nv_bfloat16*)Bf.u,
+    launch_pdl(k_moe_gateup<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __nv_bfloat16*)wgu, bvec, (const __nv_bfloat16*)Bf.u,
                                                       Bf.ecount, Bf.elist, (__nv_bfloat16*)Bf.zE, C, R.B, D.d,
                                                       D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
   else
-    k_moe_gateup<float><<<grid, 256, 0, s>>>((const float*)wgu, bvec, (const float*)Bf.u, Bf.ecount, Bf.elist,
+    launch_pdl(k_moe_gateup<float>, dim3(grid), dim3(256), 0, s, (const float*)wgu, bvec, (const float*)Bf.u, Bf.ecount, Bf.elist,
                                              (float*)Bf.zE, C, R.B, D.d, D.Fe, D.k, D.maxB, R.has_primary(),
                                              R.has_aux());
 }
@@ -674,6 +762,8 @@ template <typename T>
 __global__ void k_moe_down(const T* __restrict__ wd, const T* __restrict__ zE, const int* __restrict__ ecount,
                            const int* __restrict__ elist, float* __restrict__ yE, int d, int Fe, int k, int maxB,
                            int prim, int aux) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int e = blockIdx.x;
   int cnt = ecount[e];
   if (cnt == 0) return;
@@ -697,11 +787,11 @@ __global__ void k_moe_down(const T* __restrict__ wd, const T* __restrict__ zE, c
 void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, const Rows& R, cudaStream_t s) {
   dim3 grid(D.E, (D.d + 7) / 8);
   if (D.bf16)
-    k_moe_down<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)wd, (const __nv_bfloat16*)Bf.zE,
+    launch_pdl(k_moe_down<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __nv_bfloat16*)wd, (const __nv_bfloat16*)Bf.zE,
                                                     Bf.ecount, Bf.elist, Bf.yE, D.d, D.Fe, D.k, D.maxB,
                                                     R.has_primary(), R.has_aux());
   else
-    k_moe_down<float><<<grid, 256, 0, s>>>((const float*)wd, (const float*)Bf.zE, Bf.ecount, Bf.elist, Bf.yE, D.d,
+    launch_pdl(k_moe_down<float>, dim3(grid), dim3(256), 0, s, (const float*)wd, (const float*)Bf.zE, Bf.ecount, Bf.elist, Bf.yE, D.d,
                                            D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
 }
 
@@ -709,6 +799,8 @@ void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, c
 __global__ void k_moe_combine(const float* __restrict__ yE, const float* __restrict__ gate,
                               const float* __restrict__ cvec, float* __restrict__ h, Couple C, int B, int lo, int d,
                               int k, int maxB) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
@@ -735,7 +827,7 @@ void launch_moe_combine(const Dims& D, const Buffers& Bf, const float* cvec, con
                         cudaStream_t s) {
   int n = R.hi - R.lo;
   if (n <= 0) return;
-  k_moe_combine<<<n, 256, 0, s>>>(Bf.yE, Bf.gate, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.maxB);
+  launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, s, Bf.yE, Bf.gate, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.maxB);
 }
 
 }  // namespace df

@@ -1,29 +1,614 @@
-// Tensor-core GEMMs: placeholder until the tcgen05 kernels land.
+// Swap-AB tensor-core GEMM for the stacked-row projections of the decode
+// step, with the step's epilogues fused:
+//
+//   D^T[128 weight rows][N stacked rows] = W_tile[128][K] · X[N][K]^T
+//
+// W (the shared weight matrix) is the MMA "A" operand, 128 rows per tile,
+// K-major; X (the stacked primary + auxiliary rows, padded to N, a multiple
+// of 16) is the "B" operand.  Both are staged by TMA in the 128-byte-swizzled
+// layout through an mbarrier ring; one elected thread issues tcgen05.mma
+// (kind::f16, bf16 inputs, fp32 accumulate) into a TMEM accumulator of N
+// columns; four warps drain it with tcgen05.ld.  Every weight byte is read
+// once per step for both flows ("Mecanismos Clave": grouped execution loads
+// the weights once for both flows).
+//
+// Split-K: the K-splits of one tile form a thread-block cluster (up to 16
+// CTAs).  Each CTA leaves its partial tile in shared memory; after a cluster
+// barrier CTA r sums slice r of the tile over all ranks through distributed
+// shared memory, in rank order, and runs the epilogue on that slice.  The
+// split count targets two resident CTAs per SM (one CTA streams ~35 GB/s,
+// so a single CTA per SM cannot saturate HBM).  Results are deterministic,
+// and each column (stacked row) depends only on its own inputs, so the
+// primary rows are bit-identical whether or not the auxiliary rows are
+// present.  The first ring stages' weight tiles are requested before
+// griddepcontrol.wait (weights do not depend on the previous kernel), and
+// the epilogue's parameters (coupling-vector slice, RoPE row) are staged in
+// shared memory by the otherwise idle warps during the main loop.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cooperative_groups.h>
+#include <cstdio>
+#include <cstdlib>
+
+#include "ptx.cuh"
 #include "tc_gemm.h"
 
 namespace df {
 
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kMaxStages = 4;
+constexpr int kBK = 64;                 // K elements per stage (one 128-byte swizzle atom of bf16)
+constexpr int kBM = 128;                // weight rows per tile (MMA M)
+constexpr int kStageW = kBM * kBK * 2;  // 16 KB
+constexpr int kMaxSplit = 16;           // largest cluster (non-portable size)
+
+struct EpArgs {
+  int op;
+  int lo, hi, B;  // active stacked rows
+  int n_out;      // valid output features of the matrix
+  // QKV
+  const float* a;
+  __nv_bfloat16* kvl;  // layer block of the cache
+  const float* rope;
+  const Ctrl* ctrl;
+  float* qatt;
+  int qdim, kvdim, hd, Hkv, maxB, max_len;
+  // couplings
+  Couple C;
+  const float* bvec;
+  const float* cvec;
+  // outputs
+  float* h;
+  int d;
+  __nv_bfloat16* z;
+  int F;
+  float* logits;
+  int V;
+};
+
+// Reduced values of one (row, pair) unit: features p and p + 64 of the tile.
+struct Pair {
+  float lo, hi;
+};
+
+// Sum of the cluster's partial tiles for row m, features p and p+64, in
+// cluster-rank (K-split) order.  All remote loads are issued before the sum.
+__device__ __forceinline__ Pair reduce_pair(cg::cluster_group& cl, float* st, int S, int m, int p) {
+  if (S == 1) return Pair{st[m * kBM + p], st[m * kBM + p + 64]};
+  float a[kMaxSplit], b[kMaxSplit];
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < S) {
+      const float* r = cl.map_shared_rank(st, s);
+      a[s] = r[m * kBM + p];
+      b[s] = r[m * kBM + p + 64];
+    }
+  }
+  float x = 0.f, y = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    if (s < S) {
+      x += a[s];
+      y += b[s];
+    }
+  }
+  return Pair{x, y};
+}
+
+// Epilogue parameters of pairs [p0, p1), staged in shared memory:
+//   par[0][pp], par[1][pp]  RoPE cos/sin of pair p0+pp at position t (QKV)
+//   par[2][pp], par[3][pp]  coupling vector at features p, p+64 (a for Q
+//                           tiles, b for SwiGLU tiles, c for down tiles)
+__device__ __forceinline__ void stage_params(const EpArgs& ep, float* par, int n0, int p0, int np, int i) {
+  if (i >= np) return;
+  const int p = p0 + i, g0 = n0 + p, g1 = g0 + 64;
+  float c = 0.f, s = 0.f, x = 0.f, y = 0.f;
+  switch (ep.op) {
+    case (int)TcOp::QKV: {
+      const float* cs = ep.rope + (size_t)ep.ctrl->t * ep.hd;
+      c = cs[2 * p];
+      s = cs[2 * p + 1];
+      if (n0 < ep.qdim) {
+        x = ep.a[g0];
+        y = ep.a[g1];
+      }
+      break;
+    }
+    case (int)TcOp::SWIGLU:
+      x = ep.bvec[(n0 / kBM) * 64 + p];
+      break;
+    case (int)TcOp::DOWN:
+      if (g0 < ep.n_out) x = ep.cvec[g0];
+      if (g1 < ep.n_out) y = ep.cvec[g1];
+      break;
+    default:
+      break;
+  }
+  par[0 * 64 + i] = c;
+  par[1 * 64 + i] = s;
+  par[2 * 64 + i] = x;
+  par[3 * 64 + i] = y;
+}
+
+// Epilogue over the pairs [p0, p1) of a 128-row weight tile starting at
+// output feature n0.  Work unit: (sequence b, pair p); the unit handles the
+// primary row b and the auxiliary row B+b together, so the coupling partner
+// of an auxiliary row is at hand.  Features p and p+64 form a RoPE pair
+// (head_dim 128) or a gate/up pair (SwiGLU tiles interleave 64 gate and 64
+// up rows).
+__device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl, float* st, const float* par,
+                                         int S, int n0, int p0, int p1, int tid, int nthreads) {
+  const int np = p1 - p0;
+  const bool prim = ep.lo < ep.B, aux = ep.hi > ep.B;
+  const int B = ep.B;
+  const int t = ep.op == (int)TcOp::QKV ? ep.ctrl->t : 0;
+  for (int u = tid; u < B * np; u += nthreads) {
+    const int b = u / np, pp = u % np, p = p0 + pp;
+    Pair v1{0.f, 0.f}, v2{0.f, 0.f};
+    if (prim) v1 = reduce_pair(cl, st, S, b, p);
+    if (aux) v2 = reduce_pair(cl, st, S, B + b, p);
+    const int g0 = n0 + p, g1 = n0 + p + 64;
+    const float c = par[pp], sn = par[64 + pp], cx = par[128 + pp], cy = par[192 + pp];
+    switch (ep.op) {
+      case (int)TcOp::QKV: {
+        if (n0 < ep.qdim) {
+          if (prim) {
+            if (ep.C.save) {
+              ep.C.q1s[(size_t)b * ep.qdim + g0] = v1.lo;
+              ep.C.q1s[(size_t)b * ep.qdim + g1] = v1.hi;
+            }
+            ep.qatt[(size_t)b * ep.qdim + g0] = Num<__nv_bfloat16>::quant(v1.lo * c - v1.hi * sn);
+            ep.qatt[(size_t)b * ep.qdim + g1] = Num<__nv_bfloat16>::quant(v1.hi * c + v1.lo * sn);
+          }
+          if (aux) {
+            float q0, q1;
+            if (ep.C.saved) {
+              q0 = ep.C.q1s[(size_t)b * ep.qdim + g0];
+              q1 = ep.C.q1s[(size_t)b * ep.qdim + g1];
+            } else {
+              q0 = v1.lo;
+              q1 = v1.hi;
+            }
+            const float a0 = fmaf(cx, q0, v2.lo), a1 = fmaf(cy, q1, v2.hi);
+            const size_t m = (size_t)(B + b) * ep.qdim;
+            ep.qatt[m + g0] = Num<__nv_bfloat16>::quant(a0 * c - a1 * sn);
+            ep.qatt[m + g1] = Num<__nv_bfloat16>::quant(a1 * c + a0 * sn);
+          }
+        } else if (prim) {
+          const bool isk = n0 < ep.qdim + ep.kvdim;
+          const int g = (isk ? n0 - ep.qdim : n0 - ep.qdim - ep.kvdim) / ep.hd;
+          const size_t vofs = isk ? 0 : (size_t)ep.maxB * ep.Hkv * ep.max_len * ep.hd;
+          __nv_bfloat16* P = ep.kvl + vofs + (((size_t)b * ep.Hkv + g) * ep.max_len + t) * ep.hd;
+          if (isk) {
+            P[p] = __float2bfloat16_rn(v1.lo * c - v1.hi * sn);
+            P[p + 64] = __float2bfloat16_rn(v1.hi * c + v1.lo * sn);
+          } else {
+            P[p] = __float2bfloat16_rn(v1.lo);
+            P[p + 64] = __float2bfloat16_rn(v1.hi);
+          }
+        }
+        break;
+      }
+      case (int)TcOp::RESID: {
+        if (g0 < ep.n_out) {
+          if (prim) ep.h[(size_t)b * ep.d + g0] += v1.lo;
+          if (aux) ep.h[(size_t)(B + b) * ep.d + g0] += v2.lo;
+        }
+        if (g1 < ep.n_out) {
+          if (prim) ep.h[(size_t)b * ep.d + g1] += v1.hi;
+          if (aux) ep.h[(size_t)(B + b) * ep.d + g1] += v2.hi;
+        }
+        break;
+      }
+      case (int)TcOp::SWIGLU: {
+        const int fi = (n0 / kBM) * 64 + p;
+        const float z1 = silu_f(v1.lo) * v1.hi;
+        if (prim) {
+          if (ep.C.save) ep.C.z1s[(size_t)b * ep.F + fi] = z1;
+          ep.z[(size_t)b * ep.F + fi] = __float2bfloat16_rn(z1);
+        }
+        if (aux) {
+          const float zp = ep.C.saved ? ep.C.z1s[(size_t)b * ep.F + fi] : z1;
+          const float z2 = fmaf(cx, zp, silu_f(v2.lo) * v2.hi);
+          ep.z[(size_t)(B + b) * ep.F + fi] = __float2bfloat16_rn(z2);
+        }
+        break;
+      }
+      case (int)TcOp::DOWN: {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int gn = k ? g1 : g0;
+          if (gn >= ep.n_out) continue;
+          const float y1 = k ? v1.hi : v1.lo;
+          if (prim) {
+            if (ep.C.save) ep.C.y1s[(size_t)b * ep.d + gn] = y1;
+            ep.h[(size_t)b * ep.d + gn] += y1;
+          }
+          if (aux) {
+            const float yp = ep.C.saved ? ep.C.y1s[(size_t)b * ep.d + gn] : y1;
+            ep.h[(size_t)(B + b) * ep.d + gn] += fmaf(k ? cy : cx, yp, k ? v2.hi : v2.lo);
+          }
+        }
+        break;
+      }
+      case (int)TcOp::LOGITS: {
+        if (g0 < ep.n_out) {
+          if (prim) ep.logits[(size_t)b * ep.V + g0] = v1.lo;
+          if (aux) ep.logits[(size_t)(B + b) * ep.V + g0] = v2.lo;
+        }
+        if (g1 < ep.n_out) {
+          if (prim) ep.logits[(size_t)b * ep.V + g1] = v1.hi;
+          if (aux) ep.logits[(size_t)(B + b) * ep.V + g1] = v2.hi;
+        }
+        break;
+      }
+    }
+  }
+}
+
+// One CTA = one K-split of one 128-row weight tile; the K-splits of a tile
+// form a thread-block cluster (cluster rank = split index).
+__global__ void __launch_bounds__(128, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, int N, int kblocks,
+              int kStages, EpArgs ep, Ctrl* ctrl) {
+  extern __shared__ uint8_t smem_raw[];
+  cg::cluster_group cl = cg::this_cluster();
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_x = N * kBK * 2;
+  uint8_t* sw = base;
+  uint8_t* sx = base + kStages * kStageW;
+  float* par = reinterpret_cast<float*>(sx + kStages * stage_x);  // [4][64] epilogue parameters
+  uint64_t* full = reinterpret_cast<uint64_t*>(par + 4 * 64);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tslot + 1);  // [0] abort
+  float* st = reinterpret_cast<float*>(base);                       // [N][128] partial tile, reuses the ring
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = (int)cl.num_blocks();
+  const int split = (int)cl.block_rank();
+  const int tile = blockIdx.x / S;
+  const int kb0 = (int)((long long)split * kblocks / S), kb1 = (int)((long long)(split + 1) * kblocks / S);
+  const int nk = kb1 - kb0;
+  const uint32_t ncols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+  const int p0 = split * 64 / S, p1 = (split + 1) * 64 / S;
+
+  if (tid == 0) {
+    ptx::prefetch_tmap(&tw);
+    ptx::prefetch_tmap(&tx);
+    for (int s = 0; s < kMaxStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(done, 1);
+    flags[0] = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(tslot, ncols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer.  The weights do not depend on the previous kernel, so the
+    // first stages' weight tiles are requested before waiting for it.
+    const uint64_t pol_w = ptx::policy_evict_first();
+    const int pre = nk < kStages ? nk : kStages;
+    for (int i = 0; i < pre; ++i) {
+      ptx::mbar_arrive_expect_tx(&full[i], kStageW + stage_x);
+      ptx::tma_load_2d_hint(sw + i * kStageW, &tw, &full[i], (kb0 + i) * kBK, tile * kBM, pol_w);
+    }
+    ptx::grid_dep_wait();
+    for (int i = 0; i < pre; ++i) ptx::tma_load_2d(sx + i * stage_x, &tx, &full[i], (kb0 + i) * kBK, 0);
+    for (int i = pre; i < nk; ++i) {
+      const int s = i % kStages;
+      if (!ptx::mbar_wait(&empty[s], ((i / kStages) - 1) & 1)) {
+        flags[0] = 1;
+        latch_error(ctrl, kErrTimeout, 100);
+        break;
+      }
+      ptx::mbar_arrive_expect_tx(&full[s], kStageW + stage_x);
+      ptx::tma_load_2d_hint(sw + s * kStageW, &tw, &full[s], (kb0 + i) * kBK, tile * kBM, pol_w);
+      ptx::tma_load_2d(sx + s * stage_x, &tx, &full[s], (kb0 + i) * kBK, 0);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = ptx::idesc_bf16_f32(kBM, N);
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kStages;
+      if (!ptx::mbar_wait(&full[s], (i / kStages) & 1)) {
+        flags[0] = 1;
+        latch_error(ctrl, kErrTimeout, 101);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t a0 = ptx::smem_u32(sw + s * kStageW), b0 = ptx::smem_u32(sx + s * stage_x);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        ptx::mma_bf16(tmem, ptx::desc_sw128(a0 + kk * 32), ptx::desc_sw128(b0 + kk * 32), idesc,
+                      (i | kk) != 0 ? 1u : 0u);
+      ptx::mma_commit(&empty[s]);
+    }
+    ptx::mma_commit(done);
+  } else if (warp >= 2) {
+    // Epilogue parameters are fixed inputs (and the position t was set by an
+    // earlier step), so they are staged before the dependency resolves.
+    stage_params(ep, par, tile * kBM, p0, p1 - p0, tid - 64);
+    ptx::grid_dep_wait();
+  } else {
+    ptx::grid_dep_wait();
+  }
+  __syncwarp();
+
+  const bool ok = ptx::mbar_wait(done, 0);
+  ptx::tc_fence_after();
+  if (!ok && tid == 0) {
+    flags[0] = 1;
+    latch_error(ctrl, kErrTimeout, 102);
+  }
+  __syncthreads();
+  const bool aborted = flags[0] != 0;
+
+  if (!aborted) {
+    // TMEM -> partial tile st[column j][weight row r]
+    const int r = warp * 32 + lane;
+    for (int j0 = 0; j0 < N; j0 += 16) {
+      float v[16];
+      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + j0, v);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) st[(j0 + q) * kBM + r] = v[q];
+    }
+  }
+  ptx::tc_fence_before();
+  // Every CTA of the cluster has its partial tile in shared memory after this.
+  cl.sync();
+  ptx::grid_dep_launch();
+  if (!aborted) epilogue(ep, cl, st, par, S, tile * kBM, p0, p1, tid, 128);
+  // Keep this CTA's shared memory alive until the whole cluster has read it.
+  cl.sync();
+  if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix with a box of
+// 64 columns x box_rows rows and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int tiles_of(int n_out) { return (n_out + kBM - 1) / kBM; }
+
+// K-splits per tile (= cluster size).  Two resident CTAs per SM when each
+// split still streams at least 16 K blocks (one CTA per SM cannot saturate
+// HBM on a long K loop); otherwise one CTA per SM with clusters of at most 8,
+// since wider clusters cost more in launch, barrier and reduction than short
+// K loops gain.
+int choose_splits(int n_out, int K, int sms) {
+  const int tiles = tiles_of(n_out), kb = K / kBK;
+  int s = (2 * sms) / tiles;
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s >= 1 && kb / s >= 16) return s;
+  s = sms / tiles;
+  if (s > 8) s = 8;
+  if (s > kb / 2) s = kb / 2;
+  if (s < 1) s = 1;
+  return s;
+}
+
+// Ring depth: as many stages as fit in ~64 KB (at least 2), so that two GEMM
+// CTAs and a CTA of the neighbouring kernel fit on one SM.
+int stages_for(int N) {
+  int st = (64 * 1024) / (kStageW + N * kBK * 2);
+  if (st > kMaxStages) st = kMaxStages;
+  if (st < 2) st = 2;
+  return st;
+}
+
+size_t smem_bytes(int N) {
+  return (size_t)stages_for(N) * (kStageW + N * kBK * 2) + 1024 + 4 * 64 * 4 + 256;
+}
+
+int mpad_of(const Dims& D) { return (2 * D.maxB + 15) / 16 * 16; }
+
+}  // namespace
+
 size_t tc_tickets_needed(const Dims&) { return 1; }
+
 size_t tc_partial_floats(const Dims&) { return 1; }
-bool tc_plan_init(TcPlan& P, const Dims&, const Buffers&, const std::vector<const void*>&,
-                  const std::vector<const void*>&, const std::vector<const void*>&,
-                  const std::vector<const void*>&, const void*, std::string*) {
+
+bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector<const void*>& wqkv,
+                  const std::vector<const void*>& wo, const std::vector<const void*>& wgu,
+                  const std::vector<const void*>& wd, const void* lm_head, std::string* err) {
   P.enabled = false;
+  const char* e = getenv("DF_NO_TC");
+  if (e && e[0] == '1') return true;
+  if (!D.bf16) return true;
+  if (D.hd != 128) return true;
+  if (D.qdim % kBM || D.kvdim % kBM || D.d % kBM || D.d % kBK || D.qdim % kBK) return true;
+  if (!D.E && (D.F % kBK)) return true;
+  if (mpad_of(D) > 256) return true;
+  if (!encode_fn()) return true;
+  const int Mpad = mpad_of(D);
+  P.w_qkv.resize(D.L);
+  P.w_o.resize(D.L);
+  bool ok = true;
+  for (int l = 0; l < D.L; ++l) {
+    ok &= make_map(&P.w_qkv[l], wqkv[l], D.d, D.qkvn, kBM);
+    ok &= make_map(&P.w_o[l], wo[l], D.qdim, D.d, kBM);
+  }
+  if (!D.E) {
+    P.w_gu.resize(D.L);
+    P.w_d.resize(D.L);
+    for (int l = 0; l < D.L; ++l) {
+      ok &= make_map(&P.w_gu[l], wgu[l], D.d, 2 * D.F, kBM);
+      ok &= make_map(&P.w_d[l], wd[l], D.F, D.d, kBM);
+    }
+  }
+  ok &= make_map(&P.w_lm, lm_head, D.d, D.V, kBM);
+  if (!ok) {
+    if (err) *err = "cuTensorMapEncodeTiled failed for a weight matrix";
+    return false;
+  }
+  P.u_ptr = Bf.u;
+  P.o_ptr = Bf.o;
+  P.z_ptr = Bf.z;
+  P.mpad = Mpad;
+  cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms);
+  P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms);
+  P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms);
+  P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits(D.d, D.F, D.sms);
+  P.splits[(int)TcOp::LOGITS] = choose_splits(D.V, D.d, D.sms);
+  P.enabled = true;
+  P.dense = !D.E;
   return true;
 }
-bool tc_plan_batch(TcPlan& P, const Dims&, int B, std::string*) {
+
+bool tc_plan_batch(TcPlan& P, const Dims& D, int B, std::string* err) {
   P.B = B;
+  if (!P.enabled) return true;
+  int N = (2 * B + 15) / 16 * 16;
+  P.npad = N;
+  bool ok = make_map(&P.x_u, P.u_ptr, D.d, P.mpad, N) && make_map(&P.x_o, P.o_ptr, D.qdim, P.mpad, N);
+  if (P.dense) ok = ok && make_map(&P.x_z, P.z_ptr, D.F, P.mpad, N);
+  if (!ok && err) *err = "cuTensorMapEncodeTiled failed for an activation buffer";
+  return ok;
+}
+
+void tc_plan_free(TcPlan& P) {
+  P.w_qkv.clear();
+  P.w_o.clear();
+  P.w_gu.clear();
+  P.w_d.clear();
+}
+
+bool tc_can_run(const TcPlan& P, TcOp op) {
+  if (!P.enabled) return false;
+  if ((op == TcOp::SWIGLU || op == TcOp::DOWN) && !P.dense) return false;
   return true;
 }
-void tc_plan_free(TcPlan&) {}
-bool tc_can_run(const TcPlan& P, TcOp) { return P.enabled; }
-void tc_qkv(const TcPlan&, const Dims&, const Buffers&, const void*, const float*, void*, int, const Couple&,
-            const Rows&, cudaStream_t) {}
-void tc_resid(const TcPlan&, const Dims&, const Buffers&, const void*, const Rows&, cudaStream_t) {}
-void tc_swiglu(const TcPlan&, const Dims&, const Buffers&, const void*, const float*, const Couple&, const Rows&,
-               cudaStream_t) {}
-void tc_down(const TcPlan&, const Dims&, const Buffers&, const void*, const float*, const Couple&, const Rows&,
-             cudaStream_t) {}
-void tc_logits(const TcPlan&, const Dims&, const Buffers&, const void*, const Rows&, cudaStream_t) {}
+
+namespace {
+
+EpArgs base_args(const Dims& D, const Buffers& Bf, const Rows& R, TcOp op, int n_out) {
+  EpArgs ep{};
+  ep.op = (int)op;
+  ep.lo = R.lo;
+  ep.hi = R.hi;
+  ep.B = R.B;
+  ep.n_out = n_out;
+  ep.rope = Bf.rope;
+  ep.ctrl = Bf.ctrl;
+  ep.qatt = Bf.qatt;
+  ep.qdim = D.qdim;
+  ep.kvdim = D.kvdim;
+  ep.hd = D.hd;
+  ep.Hkv = D.Hkv;
+  ep.maxB = D.maxB;
+  ep.max_len = D.max_len;
+  ep.h = Bf.h;
+  ep.d = D.d;
+  ep.z = (__nv_bfloat16*)Bf.z;
+  ep.F = D.F;
+  ep.logits = Bf.logits;
+  ep.V = D.V;
+  return ep;
+}
+
+void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int K, const EpArgs& ep,
+            const Buffers& Bf, cudaStream_t s, int splits) {
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(tiles_of(n_out) * splits);
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = smem_bytes(P.npad);
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = splits;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  cudaLaunchKernelEx(&lc, k_tc_gemm, tw, tx, P.npad, K / kBK, stages_for(P.npad), ep, Bf.ctrl);
+}
+
+}  // namespace
+
+void tc_qkv(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const float* a, void* kv, int layer,
+            const Couple& C, const Rows& R, cudaStream_t s) {
+  (void)w;
+  EpArgs ep = base_args(D, Bf, R, TcOp::QKV, D.qkvn);
+  ep.a = a;
+  ep.C = C;
+  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
+  ep.kvl = (__nv_bfloat16*)kv + layer * layer_elems;
+  launch(P, P.w_qkv[layer], P.x_u, D.qkvn, D.d, ep, Bf, s, P.splits[(int)TcOp::QKV]);
+}
+
+void tc_resid(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const Rows& R,
+              cudaStream_t s) {
+  (void)w;
+  EpArgs ep = base_args(D, Bf, R, TcOp::RESID, D.d);
+  launch(P, P.w_o[layer], P.x_o, D.d, D.qdim, ep, Bf, s, P.splits[(int)TcOp::RESID]);
+}
+
+void tc_swiglu(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* bvec,
+               const Couple& C, const Rows& R, cudaStream_t s) {
+  (void)w;
+  EpArgs ep = base_args(D, Bf, R, TcOp::SWIGLU, 2 * D.F);
+  ep.bvec = bvec;
+  ep.C = C;
+  launch(P, P.w_gu[layer], P.x_u, 2 * D.F, D.d, ep, Bf, s, P.splits[(int)TcOp::SWIGLU]);
+}
+
+void tc_down(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* cvec,
+             const Couple& C, const Rows& R, cudaStream_t s) {
+  (void)w;
+  EpArgs ep = base_args(D, Bf, R, TcOp::DOWN, D.d);
+  ep.cvec = cvec;
+  ep.C = C;
+  launch(P, P.w_d[layer], P.x_z, D.d, D.F, ep, Bf, s, P.splits[(int)TcOp::DOWN]);
+}
+
+void tc_logits(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const Rows& R, cudaStream_t s) {
+  (void)w;
+  EpArgs ep = base_args(D, Bf, R, TcOp::LOGITS, D.V);
+  launch(P, P.w_lm, P.x_u, D.V, D.d, ep, Bf, s, P.splits[(int)TcOp::LOGITS]);
+}
 
 }  // namespace df

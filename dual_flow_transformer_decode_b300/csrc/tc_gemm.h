@@ -16,6 +16,9 @@ struct TcPlan {
   int B = 0;
   int npad = 0;                // stacked rows padded to the MMA N granule
   int splits[5] = {1, 1, 1, 1, 1};
+  bool dense = true;
+  int mpad = 0;                // rows allocated in the activation buffers
+  void *u_ptr = nullptr, *o_ptr = nullptr, *z_ptr = nullptr;
   std::vector<CUtensorMap> w_qkv, w_o, w_gu, w_d;
   CUtensorMap w_lm;
   CUtensorMap x_u, x_o, x_z;
@@ -32,11 +35,12 @@ bool tc_can_run(const TcPlan& P, TcOp op);
 
 void tc_qkv(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const float* a, void* kv, int layer,
             const Couple& C, const Rows& R, cudaStream_t s);
-void tc_resid(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const Rows& R, cudaStream_t s);
-void tc_swiglu(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const float* bvec, const Couple& C,
-               const Rows& R, cudaStream_t s);
-void tc_down(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const float* cvec, const Couple& C,
-             const Rows& R, cudaStream_t s);
+void tc_resid(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const Rows& R,
+              cudaStream_t s);
+void tc_swiglu(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* bvec,
+               const Couple& C, const Rows& R, cudaStream_t s);
+void tc_down(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* cvec,
+             const Couple& C, const Rows& R, cudaStream_t s);
 void tc_logits(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const Rows& R, cudaStream_t s);
 
 }  // namespace df

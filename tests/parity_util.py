@@ -139,10 +139,16 @@ def assert_parity(cfg, rep, max_near_tie_frac=0.25):
 
 
 def kv_compare(cfg, gpu_kv, oracle, n_pos, seqs_gpu, seqs_or=None):
-    """Max |difference| and fraction of exactly equal elements between the GPU
-    cache and the oracle's cache over positions 0..n_pos-1."""
+    """Max |difference| and RMS(difference) / RMS(value) between the GPU cache
+    and the oracle's cache over positions 0..n_pos-1.
+
+    Cache entries are stored values (bf16 in bf16 models): where the GPU's
+    fp32 and the oracle's fp64 pre-rounding values straddle a rounding
+    boundary they land one ulp apart, and such flips cascade through later
+    layers, so the bound is on the size of the differences, not on how many
+    entries are bit-equal."""
     seqs_or = seqs_or if seqs_or is not None else list(range(len(seqs_gpu)))
-    mx, eq, tot = 0.0, 0, 0
+    mx, ss_d, ss_v = 0.0, 0.0, 0.0
     for l in range(cfg.n_layers):
         for i, b in zip(seqs_or, seqs_gpu):
             for kind, arr in ((0, oracle.K), (1, oracle.V)):
@@ -150,6 +156,13 @@ def kv_compare(cfg, gpu_kv, oracle, n_pos, seqs_gpu, seqs_or=None):
                 o = arr[l][i][:, :n_pos]
                 d = np.abs(g - o)
                 mx = max(mx, float(d.max()))
-                eq += int((d == 0).sum())
-                tot += d.size
-    return mx, eq / max(tot, 1)
+                ss_d += float((d * d).sum())
+                ss_v += float((o * o).sum())
+    return mx, (ss_d / max(ss_v, 1e-300)) ** 0.5
+
+
+def assert_kv_close(cfg, mx, rel):
+    if cfg.dtype == "f32":
+        assert mx < 1e-4, (mx, rel)
+    else:
+        assert mx < 0.05 and rel < 2.0 ** -8, (mx, rel)

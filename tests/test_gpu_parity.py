@@ -7,7 +7,7 @@ import pytest
 import dfsynth
 from dfsynth.gen import Weights
 
-from parity_util import GpuRun, oracle_run, compare_steps, assert_parity, kv_compare, tied_weights
+from parity_util import GpuRun, oracle_run, compare_steps, assert_parity, kv_compare, assert_kv_close, tied_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -24,12 +24,9 @@ def test_parity_small(name, cuda_device):
     rep = compare_steps(cfg, g.steps, outs)
     print(name, {k: v for k, v in rep.items() if not isinstance(v, list)})
     assert_parity(cfg, rep)
-    mx, frac = kv_compare(cfg, g.kv, o, cfg.max_len, list(range(cfg.batch)))
-    print("kv max diff", mx, "exact fraction", frac)
-    if cfg.dtype == "f32":
-        assert mx < 1e-4
-    else:
-        assert mx < 0.05 and frac > 0.97
+    mx, rel = kv_compare(cfg, g.kv, o, cfg.max_len, list(range(cfg.batch)))
+    print("kv max diff", mx, "relative rms diff", rel)
+    assert_kv_close(cfg, mx, rel)
     g.close()
 
 
