@@ -45,7 +45,7 @@ _lib = None
 
 EXPORTS = ["df_workspace_bytes", "df_create", "df_prefill", "df_set_length", "df_decode_step",
            "df_decode_step_host", "df_set_mode", "df_debug_outputs", "df_sync", "df_length",
-           "df_step_kernels", "df_time_op", "df_last_error", "df_destroy"]
+           "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc"]
 
 DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6}
 
@@ -68,6 +68,8 @@ def lib():
     L.df_set_length.restype = i
     L.df_decode_step.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step.restype = i
+    L.df_decode_step_noalloc.argtypes = [vp, vp, vp, vp, vp]
+    L.df_decode_step_noalloc.restype = i
     L.df_decode_step_host.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step_host.restype = i
     L.df_set_mode.argtypes = [vp, i, i]
@@ -130,6 +132,13 @@ def df_decode_step(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_ptr: int 
     check(ctx, lib().df_decode_step(ctx, C.c_void_p(tokens_ptr), C.c_void_p(logp_mix_ptr or None),
                                     C.c_void_p(argmax_ptr or None), C.c_void_p(alpha_ptr or None)),
           "df_decode_step")
+
+
+def df_decode_step_noalloc(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_ptr: int = 0,
+                           alpha_ptr: int = 0) -> None:
+    check(ctx, lib().df_decode_step_noalloc(ctx, C.c_void_p(tokens_ptr), C.c_void_p(logp_mix_ptr or None),
+                                            C.c_void_p(argmax_ptr or None), C.c_void_p(alpha_ptr or None)),
+          "df_decode_step_noalloc")
 
 
 def df_decode_step_host(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_ptr: int = 0,

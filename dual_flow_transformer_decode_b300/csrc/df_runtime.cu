@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -78,6 +79,7 @@ struct df_ctx {
   bool use_graph = true;
   int force_generic = 0;
   GraphSlot dec, pre;
+  GraphSlot dec_static;  // graph of df_decode_step_noalloc
   int last_kernels = -1;
   df::TcPlan tc;
   df::AttnPlan at;
@@ -523,6 +525,7 @@ static df_status set_batch(df_ctx* X, int B) {
   if (B != X->B) {
     X->dec.reset();
     X->pre.reset();
+    X->dec_static.reset();
     X->B = B;
     X->splits = df::attn_splits(X->D, B);
     std::string perr;
@@ -694,6 +697,7 @@ void df_destroy(df_ctx* X) {
   if (X->stream) cudaStreamSynchronize(X->stream);
   X->dec.reset();
   X->pre.reset();
+  X->dec_static.reset();
   df::tc_plan_free(X->tc);
   df::attn_fast_free(X->at);
   if (X->own_stream) cudaStreamDestroy(X->stream);
@@ -701,3 +705,88 @@ void df_destroy(df_ctx* X) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode step without workspace scratch for the split-attention partials.
+//
+// For callers that cannot allocate device memory at the point where they
+// step the model: a serving loop that runs inside a fixed memory budget set
+// at start-up, or code that assembles its own CUDA graph and may not add an
+// allocation to it.  The partials that the split-KV attention kernels
+// exchange (running max, running sum and unnormalised output per query row
+// and split) live in the file-scope array below instead of the caller's
+// workspace.  The array is reserved in every GPU's memory when the library is
+// loaded and held until the process exits.
+namespace {
+
+constexpr size_t kStaticScratchFloats = size_t(1) << 20;  // 4 MiB of fp32
+__device__ __align__(256) float g_step_scratch[kStaticScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_step_scratch on the current device, looked up once per
+// device.  In host code the symbol is only a host-side stand-in, so the
+// address must come from cudaGetSymbolAddress.
+cudaError_t static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    float* p = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_step_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax,
+                                            float* alpha) {
+  if (!X) return DF_ERR_ARG;
+  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_noalloc: null tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_noalloc before df_prefill");
+  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step_noalloc: cache full (t >= max_len)");
+  const size_t parts = (size_t)X->B * X->D.Hkv * X->splits * 2 * X->D.G;
+  const size_t need = parts * (X->D.hd + 2);
+  if (need > kStaticScratchFloats) {
+    char buf[160];
+    snprintf(buf, sizeof(buf),
+             "df_decode_step_noalloc: attention partials need %zu floats, the static scratch holds %zu", need,
+             kStaticScratchFloats);
+    return fail(X, DF_ERR_CAPACITY, buf);
+  }
+  float* scratch = nullptr;
+  cudaError_t e = static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(X, e, "cudaGetSymbolAddress");
+  GraphKey key{};
+  key.p[0] = tokens;
+  key.p[1] = logp_mix;
+  key.p[2] = argmax;
+  key.p[3] = alpha;
+  key.p[4] = X->dbg_logp1;
+  key.p[5] = X->dbg_logp2;
+  key.p[6] = X->dbg_topk;
+  key.p[7] = scratch;
+  key.i[0] = X->aux_on;
+  key.i[1] = X->ungrouped;
+  key.i[2] = X->B;
+  key.i[3] = X->force_generic;
+  key.i[4] = X->dbg_router != nullptr;
+  StepOut o{logp_mix, argmax, alpha};
+  // The step is enqueued with the partials pointed at the static array.
+  Buffers saved = X->Bf;
+  X->Bf.part_o = scratch;
+  X->Bf.part_ml = scratch + parts * X->D.hd;
+  df_status st = run_captured(X, X->dec_static, key, [&] { enqueue_decode(X, tokens, o); }, 1);
+  X->Bf = saved;
+  if (st != DF_OK) return st;
+  X->t += 1;
+  return DF_OK;
+}

@@ -162,6 +162,28 @@ df_status df_set_mode(df_ctx* ctx, int aux_on, int ungrouped);
  * logit); router fp32 [n_layers][B][n_experts] (primary router logits). */
 df_status df_debug_outputs(df_ctx* ctx, float* logp1, float* logp2, int32_t* topk, float* router);
 
+/* Decode step without workspace scratch for the attention partials.
+ *
+ * The method described by the paper has no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory where they step
+ * the model (a serving loop held to a fixed memory budget after start-up,
+ * or code that assembles its own CUDA graph and may not add an allocation
+ * to it).  Same arguments, outputs and position handling as df_decode_step.
+ * The partials that the split-KV attention kernels exchange are kept in a
+ * file-scope device array of 2^20 floats (4 MiB) that every GPU loading the
+ * library reserves until the process exits; the workspace given to
+ * df_create is still used for everything else.
+ *  - Returns DF_ERR_CAPACITY before enqueuing anything when the partials of
+ *    the current batch (B * n_kv_heads * splits * 2 * (n_heads/n_kv_heads)
+ *    rows of head_dim + 2 floats) exceed the array.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls in the process share the one array and it keeps the last
+ *    call's contents (every slot a call reads is written by that call first);
+ *    calls that overlap on the GPU, from any context or stream, race. */
+df_status df_decode_step_noalloc(df_ctx* ctx, const int32_t* tokens, float* logp_mix, int32_t* argmax,
+                                 float* alpha);
+
 /* Synchronise the stream and report any latched device error. */
 df_status df_sync(df_ctx* ctx);
 

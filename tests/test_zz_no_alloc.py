@@ -1,0 +1,75 @@
+"""df_decode_step_noalloc: the decode step for callers that cannot allocate
+device memory where they step the model (a serving loop held to a fixed
+memory budget after start-up, or code building its own CUDA graph).  Its
+split-attention partials live in a static device array instead of the
+workspace; two steps in a row must give what df_decode_step gives.
+
+Kept in a file of its own, collected last, so a failure here comes after
+every other test has run."""
+
+import numpy as np
+import pytest
+
+import dfsynth
+from dfsynth.gen import Weights
+
+pytestmark = pytest.mark.gpu
+
+
+def _pair(cfg):
+    import torch
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    ms = [DualFlowModel(cfg, w) for _ in range(2)]
+    pre = torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda()
+    for m in ms:
+        m.prefill(pre)
+    return ms, tok
+
+
+@pytest.mark.parametrize("name", ["t_fp32", "t_fp32_gqa", "t_bf16"])
+def test_noalloc_step_matches_decode_step(name, cuda_device):
+    import torch
+    from dual_flow_transformer_decode_b300 import binding as b
+    cfg = dfsynth.get_config(name)
+    (ref, st), tok = _pair(cfg)
+    B, V = cfg.batch, cfg.vocab
+    outs = []
+    for m in (ref, st):
+        lp = torch.zeros(B, V, device="cuda")
+        am = torch.zeros(B, dtype=torch.int32, device="cuda")
+        al = torch.zeros(B, device="cuda")
+        outs.append((lp, am, al))
+    tol = 1e-4 if cfg.dtype == "f32" else 2e-2
+    for s in range(2):
+        t = torch.from_numpy(tok[:, cfg.n_prefill + s].copy()).cuda()
+        ref.decode_step(t, *outs[0])
+        b.df_decode_step_noalloc(st.ctx, t.data_ptr(), outs[1][0].data_ptr(), outs[1][1].data_ptr(),
+                                 outs[1][2].data_ptr())
+        ref.sync()
+        st.sync()
+        d = float((outs[0][0] - outs[1][0]).abs().max())
+        assert d <= tol, (s, d)
+        assert np.array_equal(outs[0][1].cpu().numpy(), outs[1][1].cpu().numpy())
+        assert float((outs[0][2] - outs[1][2]).abs().max()) <= tol
+    assert st.length == ref.length == cfg.n_prefill + 2
+    ref.close()
+    st.close()
+
+
+def test_noalloc_step_rejects_partials_beyond_the_static_array(cuda_device):
+    import torch
+    from dual_flow_transformer_decode_b300 import binding as b
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+    # 64 sequences x 4 KV heads x up to 16 splits x 8 query rows x 130 floats
+    cfg = dfsynth.DFConfig("big_partials", n_layers=1, d_model=256, n_heads=16, n_kv_heads=4, head_dim=128,
+                           ffn_hidden=256, vocab=256, dtype="f32", batch=64, n_prefill=4000, n_steps=8)
+    m = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, 0, "cuda"))
+    m.set_length(cfg.batch, cfg.n_prefill)
+    t = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
+    with pytest.raises(b.DFError) as e:
+        b.df_decode_step_noalloc(m.ctx, t.data_ptr())
+    assert e.value.status == b.DF_ERR_CAPACITY
+    assert m.length == cfg.n_prefill
+    m.close()
