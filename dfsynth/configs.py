@@ -120,6 +120,10 @@ TEST_CONFIGS = {
     "t_bf16_b9": DFConfig("t_bf16_b9", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                           head_dim=128, ffn_hidden=512, vocab=777, dtype="bf16",
                           batch=9, n_prefill=40, n_steps=4, gain_std=0.1),
+    # long enough that attention runs with several KV splits (a cluster merge)
+    "t_bf16_long": DFConfig("t_bf16_long", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
+                            head_dim=128, ffn_hidden=512, vocab=600, dtype="bf16",
+                            batch=2, n_prefill=1100, n_steps=3, gain_std=0.1),
     "t_moe": DFConfig("t_moe", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                       head_dim=128, ffn_hidden=0, vocab=1000, dtype="bf16",
                       batch=5, n_prefill=33, n_steps=5, n_experts=8, top_k=2,

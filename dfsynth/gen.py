@@ -19,8 +19,7 @@ from __future__ import annotations
 
 import os
 from collections import OrderedDict
-from concurrent.futures import ProcessPoolExecutor
-import multiprocessing as mp
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -109,11 +108,6 @@ def all_keys(cfg) -> list:
     return keys
 
 
-def _gen_job(args):
-    cfg, seed, key = args
-    return key, generate_tensor(cfg, seed, key)
-
-
 class Weights:
     """Lazily generated, optionally cached mapping key -> float32 array.
 
@@ -146,20 +140,16 @@ class Weights:
     def keys(self) -> list:
         return all_keys(self.cfg)
 
-    def prefetch(self, keys=None, procs: int | None = None) -> None:
-        """Generate many tensors in a spawned process pool (counter-based draws
-        make every tensor independent of the others)."""
+    def prefetch(self, keys=None, threads: int | None = None) -> None:
+        """Generate many tensors in a thread pool (counter-based draws make
+        every tensor independent of the others; numpy's generators release the
+        GIL while filling)."""
         keys = [k for k in (keys or self.keys()) if k not in self.overrides and k not in self._cache]
         if not keys:
             return
-        procs = procs or min(len(keys), len(os.sched_getaffinity(0)))
-        if procs <= 1 or len(keys) < 4:
-            for k in keys:
-                self[k]
-            return
-        ctx = mp.get_context("spawn")
-        with ProcessPoolExecutor(max_workers=procs, mp_context=ctx) as ex:
-            for key, arr in ex.map(_gen_job, [(self.cfg, self.seed, k) for k in keys], chunksize=1):
+        threads = threads or min(len(keys), len(os.sched_getaffinity(0)))
+        with ThreadPoolExecutor(max_workers=max(1, threads)) as ex:
+            for key, arr in ex.map(lambda k: (k, generate_tensor(self.cfg, self.seed, k)), keys):
                 self._cache[key] = arr
 
 

@@ -7,7 +7,7 @@
 // Grid (split, kv head, sequence); the splits of one (sequence, KV head)
 // form a thread-block cluster.  A producer warp streams 64-position K and V
 // tiles with TMA (3-D tensor map over the cache, 128-byte swizzle) through a
-// 2-stage mbarrier ring; tiles below the current position t do not depend on
+// 2-stage mbarrier ring (up to 4); tiles below the current position t do not depend on
 // the previous kernel and are requested before griddepcontrol.wait.  Each
 // tile is read from HBM once for all query rows of the KV head (up to 16:
 // G primary + G auxiliary).  Four compute warps each own 16 positions of a
@@ -42,7 +42,7 @@ namespace {
 
 constexpr int HD = 128;
 constexpr int TP = 64;            // positions per tile
-constexpr int NS = 2;             // ring stages
+constexpr int NSMAX = 4;          // ring stages (runtime NS <= NSMAX)
 constexpr int BOX = TP * 64 * 2;  // one TMA box: 64 positions x 64 dims bf16 = 8 KB
 constexpr int STAGE = 4 * BOX;    // K lo, K hi, V lo, V hi = 32 KB
 constexpr int RQ = 16;            // query rows per MMA (m16)
@@ -92,7 +92,8 @@ __device__ __forceinline__ uint32_t sw_off(int pos, int dim) {
 
 __global__ void __launch_bounds__(160, 2)
     k_attn_tma(const __grid_constant__ CUtensorMap tkv, const float* __restrict__ qatt, Ctrl* __restrict__ ctrl,
-               __nv_bfloat16* __restrict__ out, int B, int Hkv, int G, int maxB, int layer, int flo, int fhi) {
+               __nv_bfloat16* __restrict__ out, int B, int Hkv, int G, int maxB, int layer, int flo, int fhi,
+               int NS, int l2pf) {
   extern __shared__ uint8_t smem_raw[];
   cg::cluster_group cl = cg::this_cluster();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,8 +101,8 @@ __global__ void __launch_bounds__(160, 2)
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(ring + NS * STAGE);  // [16][128]
   float* cpart = reinterpret_cast<float*>(qs + RQ * HD);                   // CTA partial: M[16], L[16], O[16][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(cpart + 2 * RQ + RQ * HD);
-  uint64_t* empty = full + NS;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NS);
+  uint64_t* empty = full + NSMAX;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NSMAX);
 
   const int splits = (int)cl.num_blocks();
   const int s = (int)cl.block_rank(), g = blockIdx.y, b = blockIdx.z;
@@ -146,6 +147,15 @@ __global__ void __launch_bounds__(160, 2)
       ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[issued], 0, p0, zV);
       ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[issued], 64, p0, zV);
     }
+    if (l2pf)
+      for (int i = issued; i < ntiles; ++i) {
+        const int p0 = s0 + i * TP;
+        if (p0 + TP > t) break;
+        ptx::tma_prefetch_3d(&tkv, 0, p0, zK);
+        ptx::tma_prefetch_3d(&tkv, 64, p0, zK);
+        ptx::tma_prefetch_3d(&tkv, 0, p0, zV);
+        ptx::tma_prefetch_3d(&tkv, 64, p0, zV);
+      }
   }
   ptx::grid_dep_wait();
 
@@ -394,11 +404,11 @@ __global__ void __launch_bounds__(160, 2)
   cl.sync();
 }
 
-size_t smem_bytes() {
+size_t smem_bytes(int NS) {
   size_t ring = (size_t)NS * STAGE;
   size_t merge = (size_t)(2 * 4 * RQ + 4 * RQ * HD) * 4;  // reuses the ring after the loop
   if (merge > ring) ring = merge;
-  return 1024 + ring + (size_t)RQ * HD * 2 + (size_t)(2 * RQ + RQ * HD) * 4 + 2 * NS * 8 + 16;
+  return 1024 + ring + (size_t)RQ * HD * 2 + (size_t)(2 * RQ + RQ * HD) * 4 + 2 * NSMAX * 8 + 16;
 }
 
 }  // namespace
@@ -425,7 +435,7 @@ bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err) {
     if (err) *err = "cuTensorMapEncodeTiled failed for the KV cache";
     return false;
   }
-  cudaFuncSetAttribute(k_attn_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes());
+  cudaFuncSetAttribute(k_attn_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(NSMAX));
   cudaFuncSetAttribute(k_attn_tma, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   P.enabled = true;
   return true;
@@ -444,7 +454,11 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(splits, D.Hkv, R.B);
   lc.blockDim = dim3(160);
-  lc.dynamicSmemBytes = smem_bytes();
+  // Two ring stages: deeper rings or L2 prefetch of the split measured no
+  // faster, and two stages let two attention CTAs share an SM with a CTA of
+  // the next GEMM.
+  const int ns = 2, l2pf = 0;
+  lc.dynamicSmemBytes = smem_bytes(ns);
   lc.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -456,7 +470,7 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   lc.attrs = at;
   lc.numAttrs = 2;
   cudaLaunchKernelEx(&lc, k_attn_tma, P.kv, (const float*)Bf.qatt, Bf.ctrl, (__nv_bfloat16*)Bf.o, R.B, D.Hkv, D.G,
-                     D.maxB, layer, flo, fhi);
+                     D.maxB, layer, flo, fhi, ns, l2pf);
 }
 
 }  // namespace df

@@ -69,6 +69,10 @@ struct Buffers {
   int* elist;       // [E][maxB] entries b*k + j
   void* zE;         // [2][maxB][k][Fe] expert hidden (dtype)
   float* yE;        // [2][maxB][k][d] expert outputs fp32
+  int* eslot;       // [maxB][k] position of entry b*k+j in its expert's list
+  void* xg;         // [E][nxe][d] packed expert input rows (tensor-core MoE path)
+  void* zEt;        // [E][nxe][Fe] packed expert hidden rows
+  float* yEt;       // [E][nxe][d] packed expert outputs
   float* out_logp;  // [maxB][V] host-step staging
   int* out_arg;     // [maxB]
   float* out_alpha; // [maxB]
@@ -134,6 +138,7 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
                 float* alpha, float* logp1, float* logp2, cudaStream_t s);
 
 // MoE with router replay.
+void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s);
 void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R,
                       int32_t* dbg_topk, float* dbg_router, cudaStream_t s);
 void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu, const float* bvec,

@@ -26,6 +26,7 @@
 #include "df.h"
 #include "df_internal.h"
 #include "tc_gemm.h"
+#include "tc_moe.h"
 #include "attn_fast.h"
 
 using df::Buffers;
@@ -82,6 +83,7 @@ struct df_ctx {
   GraphSlot dec_static;  // graph of df_decode_step_noalloc
   int last_kernels = -1;
   df::TcPlan tc;
+  df::MoePlan moe;
   df::AttnPlan at;
   std::string err;
 };
@@ -119,6 +121,7 @@ bool valid_config(const df_config* c, std::string* why) {
     if (c->top_k <= 0 || c->top_k > c->n_experts || c->top_k > 16) return bad("top_k must be in [1, min(16, E)]");
     if (c->expert_hidden <= 0 || c->expert_hidden % 64) return bad("expert_hidden must be a positive multiple of 64");
   }
+  if (c->n_experts > 4096) return bad("n_experts above 4096");
   if (!(c->norm_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("norm_eps and rope_theta must be positive");
   return true;
 }
@@ -199,6 +202,11 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.elist = (int*)take((size_t)D.E * D.maxB * 4);
   b.zE = take(D.E ? 2 * (size_t)D.maxB * D.k * D.Fe * esz : 0);
   b.yE = (float*)take(D.E ? 2 * (size_t)D.maxB * D.k * D.d * 4 : 0);
+  b.eslot = (int*)take(D.E ? (size_t)D.maxB * D.k * 4 : 0);
+  const size_t nxe = D.E ? (size_t)df::moe_nxe(D) : 0;
+  b.xg = take(D.E * nxe * D.d * esz);
+  b.zEt = take(D.E * nxe * D.Fe * esz);
+  b.yEt = (float*)take(D.E * nxe * D.d * 4);
   b.out_logp = (float*)take((size_t)D.maxB * D.V * 4);
   b.out_arg = (int*)take(D.maxB * 4);
   b.out_alpha = (float*)take(D.maxB * 4);
@@ -296,11 +304,15 @@ void op_moe(df_ctx* X, int l, const Rows& R, const Couple& C) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
-  df::launch_gemv(D, X->router[l], D.E, D.d, Bf.un, D.d, 1, Bf.rlog, D.E, R, s);
+  df::launch_router(D, Bf, X->router[l], R, s);
   df::launch_moe_route(D, Bf, l, R.has_primary() ? 1 : 0, R, X->dbg_topk, X->dbg_router, s);
-  df::launch_moe_gateup_generic(D, Bf, X->wgu[l], X->b[l], C, R, s);
-  df::launch_moe_down_generic(D, Bf, X->wd[l], R, s);
-  df::launch_moe_combine(D, Bf, X->c[l], C, R, s);
+  if (!X->force_generic && X->moe.enabled) {
+    df::moe_tc_forward(X->moe, D, Bf, l, X->b[l], X->c[l], C, R, s);
+  } else {
+    df::launch_moe_gateup_generic(D, Bf, X->wgu[l], X->b[l], C, R, s);
+    df::launch_moe_down_generic(D, Bf, X->wd[l], R, s);
+    df::launch_moe_combine(D, Bf, X->c[l], C, R, s);
+  }
 }
 
 // LM head over the final-normed rows.
@@ -511,6 +523,7 @@ df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, voi
   }
   std::string perr;
   if (!df::tc_plan_init(X->tc, X->D, X->Bf, X->wqkv, X->wo, X->wgu, X->wd, X->lm_head, &perr) ||
+      (X->D.E && !df::moe_tc_init(X->moe, X->D, X->Bf, X->wgu, X->wd, &perr)) ||
       !df::attn_fast_init(X->at, X->D, X->kv, &perr)) {
     fprintf(stderr, "df_create: %s\n", perr.c_str());
     if (X->own_stream) cudaStreamDestroy(X->stream);
@@ -699,6 +712,7 @@ void df_destroy(df_ctx* X) {
   X->pre.reset();
   X->dec_static.reset();
   df::tc_plan_free(X->tc);
+  df::moe_tc_free(X->moe);
   df::attn_fast_free(X->at);
   if (X->own_stream) cudaStreamDestroy(X->stream);
   delete X;

@@ -358,22 +358,26 @@ void launch_ep_residual(const Dims& D, const Buffers& Bf, const float* raw, int 
 // unnormalised output o per query row; attn_combine merges the splits.
 // Partial slot of a query row: ((b*Hkv + g)*splits + s)*2G + f*G + j.
 
-// Splits per (sequence, KV head): the count whose CTAs fill the GPU's
-// resident slots (2 per SM) with the least wave-quantisation loss, keeping
-// at least 4 tiles of 64 positions per split at full length.
+// Splits per (sequence, KV head), at most 16 (the splits of a pair form one
+// thread-block cluster).  Chosen by a simple time model over the cache
+// length T (in 64-position tiles): with `slots` = 2 resident CTAs per SM,
+//   time(s) = waves(s) * (c0 + ceil(T / s) * c_tile),
+//   waves(s) = ceil(pairs * s / slots),
+// where c0 (~4 us) is a CTA's fixed cost (barrier set-up, query load, split
+// merge) and c_tile (~1.5 us) the time to stream one 32 KB K+V tile at a
+// CTA's fair share of HBM bandwidth.
 int attn_splits(const Dims& D, int B) {
   const int pairs = B * D.Hkv;
   const int slots = 2 * D.sms;
-  int maxs = D.max_len / 256;
-  if (maxs < 1) maxs = 1;
-  if (maxs > 16) maxs = 16;  // the splits of a (sequence, KV head) form one thread-block cluster
+  const int T = (D.max_len + 63) / 64;
+  const double c0 = 4.0, c_tile = 1.5;
   int best = 1;
-  double best_eff = -1.0;
-  for (int s = 1; s <= maxs; ++s) {
-    double x = (double)pairs * s / slots;
-    double eff = x / std::ceil(x);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+  double best_t = 1e30;
+  for (int s = 1; s <= 16 && s <= T; ++s) {
+    const double waves = std::ceil((double)pairs * s / slots);
+    const double tm = waves * (c0 + std::ceil((double)T / s) * c_tile);
+    if (tm < best_t - 1e-9) {
+      best_t = tm;
       best = s;
     }
   }
@@ -639,6 +643,46 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
 }
 
 // ------------------------------------------------------------------ MoE (router replay)
+// Router logits r[m][e] = Wr[e] · un[m] with the normed row unrounded (fp32)
+// and Wr stored in the weight type: one CTA per stacked row holds the row in
+// shared memory; warp w computes experts w, w+8, ... with 16-byte weight loads.
+template <typename TW>
+__global__ void k_router(const TW* __restrict__ Wr, const float* __restrict__ un, float* __restrict__ rlog, int E,
+                         int d, int lo) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  extern __shared__ float xrow[];
+  const int m = lo + blockIdx.x;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) xrow[i] = un[(size_t)m * d + i];
+  __syncthreads();
+  const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int VEC = 16 / sizeof(TW);
+  for (int e = w; e < E; e += warps) {
+    const TW* wr = Wr + (size_t)e * d;
+    float acc = 0.f;
+    for (int k0 = lane * VEC; k0 < d; k0 += 32 * VEC) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(wr + k0);
+      const TW* wv = reinterpret_cast<const TW*>(&raw);
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) acc = fmaf(Num<TW>::to_f(wv[q]), xrow[k0 + q], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) rlog[(size_t)m * E + e] = acc;
+  }
+}
+
+void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s) {
+  const int n = R.hi - R.lo;
+  if (n <= 0) return;
+  const size_t smem = (size_t)D.d * sizeof(float);
+  if (D.bf16)
+    launch_pdl(k_router<__nv_bfloat16>, dim3(n), dim3(256), smem, s, (const __nv_bfloat16*)Wr, (const float*)Bf.un,
+               Bf.rlog, D.E, D.d, R.lo);
+  else
+    launch_pdl(k_router<float>, dim3(n), dim3(256), smem, s, (const float*)Wr, (const float*)Bf.un, Bf.rlog, D.E,
+               D.d, R.lo);
+}
+
 // The primary rows choose their top-k experts (descending router logit,
 // ties to the lower index); each flow's gates are the softmax of its own
 // router logits over that set ("Mecanismos Clave", Replay de Router).  The
@@ -646,48 +690,75 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
 // weights be read once for both flows.
 
 __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, float* __restrict__ gate,
-                            int* __restrict__ ecount, int* __restrict__ elist, int B, int E, int k, int maxB,
-                            int select, int prim, int aux, int32_t* __restrict__ dbg_topk_l,
+                            int* __restrict__ ecount, int* __restrict__ elist, int* __restrict__ eslot, int B, int E,
+                            int k, int maxB, int select, int prim, int aux, int32_t* __restrict__ dbg_topk_l,
                             float* __restrict__ dbg_router_l) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+  const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // one warp per primary row: k rounds of a warp-wide argmax (larger value
+  // wins, equal values -> lower index) over the experts not yet taken
+  for (int b = w; b < B; b += warps) {
     if (select) {
       const float* r = rlog + (size_t)b * E;
+      unsigned long long taken_lo = 0ull, taken_hi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
       for (int j = 0; j < k; ++j) {
         float best = -INFINITY;
-        int bi = -1;
-        for (int e = 0; e < E; ++e) {
-          bool taken = false;
-          for (int jj = 0; jj < j; ++jj) taken |= (topk_l[b * k + jj] == e);
-          if (taken) continue;
-          if (bi < 0 || r[e] > best) {
-            best = r[e];
+        int bi = 0x7fffffff;
+        int q = 0;
+        for (int e = lane; e < E; e += 32, ++q) {
+          const bool tk = q < 64 ? ((taken_lo >> q) & 1ull) : ((taken_hi >> (q - 64)) & 1ull);
+          if (tk) continue;
+          const float v = r[e];
+          if (v > best || (v == best && e < bi)) {
+            best = v;
             bi = e;
           }
         }
-        topk_l[b * k + j] = bi;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (ov > best || (ov == best && oi < bi)) {
+            best = ov;
+            bi = oi;
+          }
+        }
+        if (lane == 0) topk_l[b * k + j] = bi;
+        if (bi != 0x7fffffff && (bi % 32) == lane) {
+          const int qq = bi / 32;
+          if (qq < 64)
+            taken_lo |= 1ull << qq;
+          else
+            taken_hi |= 1ull << (qq - 64);
+        }
       }
     }
-    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
-      const float* r = rlog + (size_t)(f * B + b) * E;
-      float mx = -INFINITY;
-      for (int j = 0; j < k; ++j) mx = fmaxf(mx, r[topk_l[b * k + j]]);
-      float den = 0.f;
-      for (int j = 0; j < k; ++j) den += expf(r[topk_l[b * k + j]] - mx);
-      for (int j = 0; j < k; ++j) gate[(size_t)(f * B + b) * k + j] = expf(r[topk_l[b * k + j]] - mx) / den;
+    __syncwarp();
+    if (lane == 0) {
+      for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+        const float* r = rlog + (size_t)(f * B + b) * E;
+        float mx = -INFINITY;
+        for (int j = 0; j < k; ++j) mx = fmaxf(mx, r[topk_l[b * k + j]]);
+        float den = 0.f;
+        for (int j = 0; j < k; ++j) den += expf(r[topk_l[b * k + j]] - mx);
+        for (int j = 0; j < k; ++j) gate[(size_t)(f * B + b) * k + j] = expf(r[topk_l[b * k + j]] - mx) / den;
+      }
+      if (dbg_topk_l && prim)
+        for (int j = 0; j < k; ++j) dbg_topk_l[b * k + j] = topk_l[b * k + j];
     }
-    if (dbg_topk_l && prim)
-      for (int j = 0; j < k; ++j) dbg_topk_l[b * k + j] = topk_l[b * k + j];
     if (dbg_router_l && prim)
-      for (int e = 0; e < E; ++e) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
+      for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int cnt = 0;
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < k; ++j)
-        if (topk_l[b * k + j] == e) elist[(size_t)e * maxB + cnt++] = b * k + j;
+        if (topk_l[b * k + j] == e) {
+          eslot[b * k + j] = cnt;
+          elist[(size_t)e * maxB + cnt++] = b * k + j;
+        }
     ecount[e] = cnt;
   }
 }
@@ -695,7 +766,8 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
 void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
                       float* dbg_router, cudaStream_t s) {
   int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_route, dim3(1), dim3(256), 0, s, Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, R.B, D.E, D.k, D.maxB, select,
+  launch_pdl(k_moe_route, dim3(1), dim3(1024), 0, s, Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, Bf.eslot, R.B, D.E,
+             D.k, D.maxB, select,
                                 R.has_primary(), R.has_aux(),
                                 dbg_topk ? dbg_topk + (size_t)layer * R.B * D.k : nullptr,
                                 dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);

@@ -262,7 +262,11 @@ __global__ void __launch_bounds__(128, 1)
   const int stage_x = N * kBK * 2;
   uint8_t* sw = base;
   uint8_t* sx = base + kStages * kStageW;
-  float* par = reinterpret_cast<float*>(sx + kStages * stage_x);  // [4][64] epilogue parameters
+  // the epilogue's partial tile [N][128] fp32 reuses the ring; the region is
+  // the larger of the two
+  size_t region = (size_t)kStages * (kStageW + stage_x);
+  if ((size_t)N * kBM * 4 > region) region = (size_t)N * kBM * 4;
+  float* par = reinterpret_cast<float*>(base + region);  // [4][64] epilogue parameters
   uint64_t* full = reinterpret_cast<uint64_t*>(par + 4 * 64);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
@@ -410,16 +414,17 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
 
 int tiles_of(int n_out) { return (n_out + kBM - 1) / kBM; }
 
-// K-splits per tile (= cluster size).  Two resident CTAs per SM when each
-// split still streams at least 16 K blocks (one CTA per SM cannot saturate
-// HBM on a long K loop); otherwise one CTA per SM with clusters of at most 8,
-// since wider clusters cost more in launch, barrier and reduction than short
-// K loops gain.
-int choose_splits(int n_out, int K, int sms) {
+// K-splits per tile (= cluster size).  `per_sm` CTAs fit on an SM (from the
+// shared-memory footprint).  With two per SM, use them when each split still
+// streams at least 16 K blocks (one CTA per SM cannot saturate HBM on a long
+// K loop); otherwise aim at one wave of one CTA per SM with clusters of at
+// most 8, since wider clusters cost more in launch, barrier and reduction
+// than short K loops gain.
+int choose_splits(int n_out, int K, int sms, int per_sm) {
   const int tiles = tiles_of(n_out), kb = K / kBK;
-  int s = (2 * sms) / tiles;
+  int s = (per_sm >= 2 ? 2 * sms : sms) / tiles;
   if (s > kMaxSplit) s = kMaxSplit;
-  if (s >= 1 && kb / s >= 16) return s;
+  if (per_sm >= 2 && s >= 1 && kb / s >= 16) return s;
   s = sms / tiles;
   if (s > 8) s = 8;
   if (s > kb / 2) s = kb / 2;
@@ -437,7 +442,9 @@ int stages_for(int N) {
 }
 
 size_t smem_bytes(int N) {
-  return (size_t)stages_for(N) * (kStageW + N * kBK * 2) + 1024 + 4 * 64 * 4 + 256;
+  size_t region = (size_t)stages_for(N) * (kStageW + N * kBK * 2);
+  if ((size_t)N * kBM * 4 > region) region = (size_t)N * kBM * 4;  // epilogue partial tile
+  return region + 1024 + 4 * 64 * 4 + 256;
 }
 
 int mpad_of(const Dims& D) { return (2 * D.maxB + 15) / 16 * 16; }
@@ -487,11 +494,6 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   P.mpad = Mpad;
   cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms);
-  P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms);
-  P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms);
-  P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits(D.d, D.F, D.sms);
-  P.splits[(int)TcOp::LOGITS] = choose_splits(D.V, D.d, D.sms);
   P.enabled = true;
   P.dense = !D.E;
   return true;
@@ -502,6 +504,13 @@ bool tc_plan_batch(TcPlan& P, const Dims& D, int B, std::string* err) {
   if (!P.enabled) return true;
   int N = (2 * B + 15) / 16 * 16;
   P.npad = N;
+  // the split plan depends on how many CTAs of this N fit on one SM
+  const int per_sm = (int)((227 * 1024) / (smem_bytes(N) + 1024));
+  P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms, per_sm);
+  P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms, per_sm);
+  P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms, per_sm);
+  P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits(D.d, D.F, D.sms, per_sm);
+  P.splits[(int)TcOp::LOGITS] = choose_splits(D.V, D.d, D.sms, per_sm);
   bool ok = make_map(&P.x_u, P.u_ptr, D.d, P.mpad, N) && make_map(&P.x_o, P.o_ptr, D.qdim, P.mpad, N);
   if (P.dense) ok = ok && make_map(&P.x_z, P.z_ptr, D.F, P.mpad, N);
   if (!ok && err) *err = "cuTensorMapEncodeTiled failed for an activation buffer";

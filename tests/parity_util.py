@@ -25,7 +25,12 @@ class GpuRun:
     """Runs prefill + teacher-forced decode steps through the C-ABI and keeps
     every step's outputs on the host."""
 
-    def __init__(self, cfg, weights, tok, aux=True, ungrouped=False, steps=None, debug=True, max_len=None):
+    def __init__(self, cfg, weights, tok, aux=True, ungrouped=False, steps=None, debug=True, max_len=None,
+                 synth_sample=None, seed=0, keep_kv=True):
+        """synth_sample: None -> the GPU prefills the prompt itself; a list of
+        sequence indices -> the cache is filled with the seeded synthetic
+        blocks for those sequences (device noise for the others) and the
+        position is set to n_prefill."""
         import torch
         from dual_flow_transformer_decode_b300.model import DualFlowModel
         self.cfg = cfg
@@ -45,7 +50,11 @@ class GpuRun:
             self.m.debug_outputs(l1, l2 if aux else None, tk if cfg.n_experts else None,
                                  rl if cfg.n_experts else None)
         tok_d = torch.from_numpy(np.ascontiguousarray(tok)).to(dev)
-        self.m.prefill(tok_d[:, :cfg.n_prefill].contiguous())
+        if synth_sample is None:
+            self.m.prefill(tok_d[:, :cfg.n_prefill].contiguous())
+        else:
+            fill_synthetic_cache(cfg, self.m, synth_sample, seed)
+            self.m.set_length(B, cfg.n_prefill)
         self.steps = []
         step_tok = torch.zeros(B, dtype=torch.int32, device=dev)
         for s in range(steps if steps is not None else cfg.n_steps):
@@ -60,10 +69,45 @@ class GpuRun:
                 r["topk"] = tk.cpu().numpy().astype(np.int64)
                 r["router1"] = rl.double().cpu().numpy()
             self.steps.append(r)
-        self.kv = self.m.kv_view().float().cpu().numpy()
+        if keep_kv:
+            self.kv = self.m.kv_view().float().cpu().numpy()
+        else:
+            kvv = self.m.kv_view()
+            self.kv_new = {b: kvv[:, :, b, :, cfg.n_prefill:cfg.n_prefill + len(self.steps)].float().cpu().numpy()
+                           for b in (synth_sample or [])}
 
     def close(self):
         self.m.close()
+
+
+def fill_synthetic_cache(cfg, model, sample, seed=0):
+    """Cache positions 0..n_prefill-1: seeded synthetic blocks for the sampled
+    sequences, device noise of the same scale for the rest."""
+    import torch
+    from dfsynth.gen import synthetic_kv_block
+    kv = model.kv_view()
+    g = torch.Generator(device=kv.device)
+    g.manual_seed(1234 + seed)
+    P = cfg.n_prefill
+    for l in range(cfg.n_layers):
+        kv[l, :, :, :, :P].normal_(generator=g)
+        for b in sample:
+            K, V = synthetic_kv_block(cfg, seed, l, b, P)
+            kv[l, 0, b, :, :P] = torch.from_numpy(K).to(device=kv.device, dtype=kv.dtype)
+            kv[l, 1, b, :, :P] = torch.from_numpy(V).to(device=kv.device, dtype=kv.dtype)
+
+
+def oracle_run_synthetic(cfg, weights, tok, sample, steps, seed=0):
+    """The oracle on the sampled sequences, starting from the same synthetic cache."""
+    from dfsynth.gen import synthetic_kv_block
+    o = Oracle(cfg, weights, len(sample), max_len=cfg.max_len)
+    for i, b in enumerate(sample):
+        for l in range(cfg.n_layers):
+            K, V = synthetic_kv_block(cfg, seed, l, b, cfg.n_prefill)
+            o.set_cache(i, l, K, V)
+    o.set_length(cfg.n_prefill)
+    outs = [o.decode_step(tok[sample, cfg.n_prefill + s]) for s in range(steps)]
+    return o, outs
 
 
 def oracle_run(cfg, weights, tok, steps=None, aux=True):
@@ -128,6 +172,9 @@ def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
 
 
 def assert_parity(cfg, rep, max_near_tie_frac=0.25):
+    """max_near_tie_frac=None: near ties are only required to be valid (at
+    full size the logits of a random-weight model over 32000 tokens are so
+    flat that most argmax margins lie inside 2*eps)."""
     tol = rep["tol"]
     assert rep["max_dlogp_mix"] <= tol, rep
     assert rep["max_dlogp1"] <= tol, rep
@@ -135,7 +182,8 @@ def assert_parity(cfg, rep, max_near_tie_frac=0.25):
     assert not rep["topk_mismatch"], rep["topk_mismatch"][:5]
     assert not rep["invalid_near_ties"], rep["invalid_near_ties"][:5]
     # near ties are allowed but must stay a minority of the compared decisions
-    assert len(rep["near_ties"]) <= max_near_tie_frac * max(rep["decisions"], 1), rep["near_ties"][:5]
+    if max_near_tie_frac is not None:
+        assert len(rep["near_ties"]) <= max_near_tie_frac * max(rep["decisions"], 1), rep["near_ties"][:5]
 
 
 def kv_compare(cfg, gpu_kv, oracle, n_pos, seqs_gpu, seqs_or=None):
@@ -166,3 +214,91 @@ def assert_kv_close(cfg, mx, rel):
         assert mx < 1e-4, (mx, rel)
     else:
         assert mx < 0.05 and rel < 2.0 ** -8, (mx, rel)
+
+
+def topk_of(r, k):
+    """Top-k indices of one row, descending, equal values by ascending index."""
+    return sorted(range(len(r)), key=lambda e: (-float(r[e]), e))[:k]
+
+
+def compare_moe_steps(cfg, gpu_steps, ora_steps, seq_map):
+    """MoE comparison that follows each sampled token until its routing
+    legitimately diverges.
+
+    Per (step, token), layers in order: a routing decision whose oracle
+    margin exceeds 2*eps (eps = max |router deviation| of that row) must
+    match exactly; at a near tie the GPU's set must be a valid choice (its
+    weakest expert within 2*eps of the oracle's), and if it differs the token
+    is marked diverged: from that layer on, and in later steps, it follows
+    another (equally valid) computation and its values are not compared.
+    Undiverged (step, token) pairs are compared like dense ones.  The GPU's
+    routing is also checked against its own router logits, exactly, for
+    every layer of every token."""
+    rep = {"max_dlogp_mix": 0.0, "max_dlogp1": 0.0, "argmax_mismatch": [], "near_ties": [],
+           "invalid_near_ties": [], "topk_mismatch": [], "self_inconsistent": [], "max_drouter_undiverged": 0.0,
+           "pairs_compared": 0, "pairs_diverged": 0, "diverged_at": [], "decisions": 0}
+    k = cfg.top_k
+    diverged = [False] * len(seq_map)
+    for s, (g, o) in enumerate(zip(gpu_steps, ora_steps)):
+        for i, b in enumerate(seq_map):
+            for l in range(cfg.n_layers):
+                if list(g["topk"][l, b]) != topk_of(g["router1"][l, b], k):
+                    rep["self_inconsistent"].append((s, l, i))
+                if diverged[i]:
+                    continue
+                eps = float(np.abs(g["router1"][l, b] - o["router1"][l][i]).max())
+                rep["max_drouter_undiverged"] = max(rep["max_drouter_undiverged"], eps)
+                rep["decisions"] += 1
+                gs, os_ = list(g["topk"][l, b]), list(o["topk"][l, i])
+                if o["topk_margin"][l, i] > 2 * eps:
+                    if set(gs) != set(os_):
+                        rep["topk_mismatch"].append((s, l, i, gs, os_, float(o["topk_margin"][l, i]), eps))
+                else:
+                    rep["near_ties"].append(("topk", s, l, i, float(o["topk_margin"][l, i]), eps))
+                    r = o["router1"][l][i]
+                    if r[os_].min() - r[gs].min() > 2 * eps:
+                        rep["invalid_near_ties"].append(("topk", s, l, i, gs, os_))
+                    if set(gs) != set(os_):
+                        diverged[i] = True
+                        rep["diverged_at"].append((s, l, i))
+            if diverged[i]:
+                rep["pairs_diverged"] += 1
+                continue
+            rep["pairs_compared"] += 1
+            dmix = np.abs(g["logp_mix"][b] - o["logp_mix"][i])
+            rep["max_dlogp_mix"] = max(rep["max_dlogp_mix"], float(dmix.max()))
+            rep["max_dlogp1"] = max(rep["max_dlogp1"], float(np.abs(g["logp1"][b] - o["logp1"][i]).max()))
+            eps = float(dmix.max())
+            ga, oa = int(g["argmax"][b]), int(o["argmax"][i])
+            if o["argmax_margin"][i] <= 2 * eps:
+                if o["logp_mix"][i][oa] - o["logp_mix"][i][ga] > 2 * eps:
+                    rep["invalid_near_ties"].append(("argmax", s, i, ga, oa))
+            elif ga != oa:
+                rep["argmax_mismatch"].append((s, i, ga, oa))
+    return rep
+
+
+def kv_spread_bounds(name):
+    """Full-size K/V bounds: the small-case bounds, or three times the oracle's
+    own spread on the appended K/V, whichever is larger."""
+    import json, os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_spread.json")
+    rec = json.load(open(path))[name]
+    return max(0.05, 3.0 * rec.get("kv_max", 0.0)), max(2.0 ** -8, 3.0 * rec.get("kv_rel_rms", 0.0))
+
+
+def spread_tolerance(name, base):
+    """Full-size tolerance: the benchmark spec bound, or three times the fp64 oracle's
+    own spread under 1e-7 relative perturbations before its bf16 roundings
+    (tests/golden/oracle_spread.json), whichever is larger."""
+    import json, os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_spread.json")
+    table = json.load(open(path))
+    rec = table[name]
+    spread = rec["max_dlogp_mix"]
+    if rec.get("pairs_compared", 4) < 4:
+        # MoE: the perturbed oracle itself takes the other branch of most
+        # near-tie routings, leaving too few undiverged pairs to measure a
+        # spread; use the dense model of the same width, depth and attention.
+        spread = max(spread, table["dense1b_ctx1k"]["max_dlogp_mix"])
+    return max(base, 3.0 * spread), spread

@@ -62,9 +62,10 @@ def test_noalloc_step_rejects_partials_beyond_the_static_array(cuda_device):
     import torch
     from dual_flow_transformer_decode_b300 import binding as b
     from dual_flow_transformer_decode_b300.model import DualFlowModel
-    # 64 sequences x 4 KV heads x up to 16 splits x 8 query rows x 130 floats
+    # 512 sequences x 4 KV heads x at least one split x 8 query rows x 130
+    # floats = 2.1e6 floats, beyond the 2^20 of the static array
     cfg = dfsynth.DFConfig("big_partials", n_layers=1, d_model=256, n_heads=16, n_kv_heads=4, head_dim=128,
-                           ffn_hidden=256, vocab=256, dtype="f32", batch=64, n_prefill=4000, n_steps=8)
+                           ffn_hidden=256, vocab=256, dtype="f32", batch=512, n_prefill=60, n_steps=4)
     m = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, 0, "cuda"))
     m.set_length(cfg.batch, cfg.n_prefill)
     t = torch.zeros(cfg.batch, dtype=torch.int32, device="cuda")
