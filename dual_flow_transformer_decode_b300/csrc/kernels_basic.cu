@@ -13,6 +13,8 @@
 
 #include <cmath>
 
+#include <cooperative_groups.h>
+
 #include "df_internal.h"
 #include "ptx.cuh"
 
@@ -46,9 +48,18 @@ bool pdl_enabled() {
   return v == 1;
 }
 
+constexpr int kRouterRows = 4;  // stacked rows per router CTA
+template <typename TW, int R>
+__global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const float* __restrict__ un,
+                                                float* __restrict__ rlog, int E, int d, int lo, int hi);
+
 void kernels_init() {
   cudaFuncSetAttribute(k_attn_generic<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   cudaFuncSetAttribute(k_attn_generic<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(k_router<__nv_bfloat16, kRouterRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kRouterRows * 8192 * 4);
+  cudaFuncSetAttribute(k_router<float, kRouterRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       kRouterRows * 8192 * 4);
 }
 
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { launch_pdl(k_set_pos, dim3(1), dim3(1), 0, s, c, t); }
@@ -550,47 +561,122 @@ __device__ __forceinline__ float logaddexp_f(float x, float y) {
   return mx + log1pf(expf(mn - mx));
 }
 
-__global__ void k_mix(const float* __restrict__ logits, int B, int V, int aux_on, float* __restrict__ logp_mix,
-                      int32_t* __restrict__ argmax, float* __restrict__ alpha_out, float* __restrict__ logp1,
-                      float* __restrict__ logp2) {
+// One cluster of kMixCl CTAs per sequence; CTA r handles the r-th chunk of
+// the vocabulary for both flows.  Pass 1 keeps, per thread, online softmax
+// statistics relative to a running maximum: flow 1 (max, sum e, sum e^2),
+// flow 2 (max, sum e).  The CTAs exchange their block totals through
+// distributed shared memory and every CTA merges them in rank order, so all
+// of them hold the same row totals.  Pass 2 writes the log-probabilities and
+// the per-CTA argmax; rank 0 merges those in rank order.
+constexpr int kMixCl = 8;
+constexpr int kMixThreads = 256;
+
+struct MixStat {
+  float m1, s1, q1, m2, s2;
+};
+
+__device__ __forceinline__ void mix_merge(float& m, float& s, float& q, float mo, float so, float qo) {
+  if (mo == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = mo;
+    s = so;
+    q = qo;
+    return;
+  }
+  const float mn = fmaxf(m, mo);
+  const float ea = expf(m - mn), eb = expf(mo - mn);
+  s = s * ea + so * eb;
+  q = q * ea * ea + qo * eb * eb;
+  m = mn;
+}
+
+__device__ __forceinline__ void mix_merge(MixStat& a, const MixStat& o) {
+  mix_merge(a.m1, a.s1, a.q1, o.m1, o.s1, o.q1);
+  float dummy = 0.f;
+  mix_merge(a.m2, a.s2, dummy, o.m2, o.s2, 0.f);
+}
+
+__device__ __forceinline__ void mix_push(float& m, float& s, float& q, float x) {
+  if (x > m) {
+    const float r = expf(m - x);
+    s = s * r + 1.f;
+    q = q * r * r + 1.f;
+    m = x;
+  } else {
+    const float e = expf(x - m);
+    s += e;
+    q += e * e;
+  }
+}
+
+__device__ __forceinline__ void argmax_merge(float& best, int& bi, float ov, int oi) {
+  if (ov > best || (ov == best && oi < bi)) {
+    best = ov;
+    bi = oi;
+  }
+}
+
+__global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ logits, int B, int V, int aux_on,
+                                                     float* __restrict__ logp_mix, int32_t* __restrict__ argmax,
+                                                     float* __restrict__ alpha_out, float* __restrict__ logp1,
+                                                     float* __restrict__ logp2) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ MixStat wstat[kMixThreads / 32];
+  __shared__ MixStat cstat;  // this CTA's block total, read by the whole cluster
+  __shared__ float cbest;
+  __shared__ int cidx;
+  __shared__ float wbest[kMixThreads / 32];
+  __shared__ int widx[kMixThreads / 32];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  __shared__ float red[32];
-  __shared__ float redv[32];
-  __shared__ int redi[32];
-  int b = blockIdx.x;
+  const int b = blockIdx.y;
+  const int r = (int)cl.block_rank();
+  const int chunk = (V + kMixCl - 1) / kMixCl;
+  const int v0 = r * chunk, v1 = min(V, v0 + chunk);
   const float* l1 = logits + (size_t)b * V;
   const float* l2 = logits + (size_t)(B + b) * V;
-  float m1 = -INFINITY, m2 = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    m1 = fmaxf(m1, l1[v]);
-    if (aux_on) m2 = fmaxf(m2, l2[v]);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+
+  MixStat st{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+  for (int v = v0 + threadIdx.x; v < v1; v += kMixThreads) {
+    mix_push(st.m1, st.s1, st.q1, l1[v]);
+    if (aux_on) {
+      float dummy = 0.f;
+      mix_push(st.m2, st.s2, dummy, l2[v]);
+    }
   }
-  m1 = block_max(m1, red);
-  if (aux_on) m2 = block_max(m2, red);
-  float s1 = 0.f, q1 = 0.f, s2 = 0.f;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    float e = expf(l1[v] - m1);
-    s1 += e;
-    q1 += e * e;
-    if (aux_on) s2 += expf(l2[v] - m2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MixStat ot{__shfl_xor_sync(0xffffffffu, st.m1, o), __shfl_xor_sync(0xffffffffu, st.s1, o),
+               __shfl_xor_sync(0xffffffffu, st.q1, o), __shfl_xor_sync(0xffffffffu, st.m2, o),
+               __shfl_xor_sync(0xffffffffu, st.s2, o)};
+    mix_merge(st, ot);
   }
-  s1 = block_sum(s1, red);
-  q1 = block_sum(q1, red);
-  if (aux_on) s2 = block_sum(s2, red);
-  float lse1 = m1 + logf(s1);
-  float lse2 = aux_on ? m2 + logf(s2) : 0.f;
-  float coll = q1 / (s1 * s1);
-  float alpha = aux_on ? 0.5f + 0.5f * coll : 1.0f;
-  float la = logf(alpha);
-  float lb = (alpha < 1.0f) ? log1pf(-alpha) : -INFINITY;
+  if (lane == 0) wstat[w] = st;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    MixStat t = wstat[0];
+    for (int i = 1; i < kMixThreads / 32; ++i) mix_merge(t, wstat[i]);
+    cstat = t;
+  }
+  cl.sync();
+  MixStat tot = *cl.map_shared_rank(&cstat, 0);
+  for (int i = 1; i < kMixCl; ++i) mix_merge(tot, *cl.map_shared_rank(&cstat, i));
+
+  const float lse1 = tot.m1 + logf(tot.s1);
+  const float lse2 = aux_on ? tot.m2 + logf(tot.s2) : 0.f;
+  const float coll = tot.q1 / (tot.s1 * tot.s1);
+  const float alpha = aux_on ? 0.5f + 0.5f * coll : 1.0f;
+  const float la = logf(alpha);
+  const float lb = (alpha < 1.0f) ? log1pf(-alpha) : -INFINITY;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    float lp1 = l1[v] - lse1;
+  for (int v = v0 + threadIdx.x; v < v1; v += kMixThreads) {
+    const float lp1 = l1[v] - lse1;
     float lm = lp1;
     if (aux_on) {
-      float lp2 = l2[v] - lse2;
+      const float lp2 = l2[v] - lse2;
       lm = logaddexp_f(la + lp1, lb + lp2);
       if (logp2) logp2[(size_t)b * V + v] = lp2;
     }
@@ -601,86 +687,103 @@ __global__ void k_mix(const float* __restrict__ logits, int B, int V, int aux_on
       bi = v;
     }
   }
-  // block argmax: larger value wins, equal values -> lower index
-  int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) {
-      best = ov;
-      bi = oi;
-    }
-  }
-  __syncthreads();
+  for (int o = 16; o > 0; o >>= 1)
+    argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
   if (lane == 0) {
-    redv[w] = best;
-    redi[w] = bi;
+    wbest[w] = best;
+    widx[w] = bi;
   }
   __syncthreads();
-  if (w == 0) {
-    best = lane < nw ? redv[lane] : -INFINITY;
-    bi = lane < nw ? redi[lane] : 0x7fffffff;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > best || (ov == best && oi < bi)) {
-        best = ov;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      if (argmax) argmax[b] = bi;
-      if (alpha_out) alpha_out[b] = alpha;
-    }
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < kMixThreads / 32; ++i) argmax_merge(best, bi, wbest[i], widx[i]);
+    cbest = best;
+    cidx = bi;
   }
+  cl.sync();
+  if (r == 0 && threadIdx.x == 0) {
+    float cb = cbest;
+    int ci = cidx;
+    for (int i = 1; i < kMixCl; ++i) argmax_merge(cb, ci, *cl.map_shared_rank(&cbest, i), *cl.map_shared_rank(&cidx, i));
+    if (argmax) argmax[b] = ci;
+    if (alpha_out) alpha_out[b] = alpha;
+  }
+  // keep every CTA's shared memory alive until rank 0 has read it
+  cl.sync();
 }
 
 void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax, float* alpha,
                 float* logp1, float* logp2, cudaStream_t s) {
-  launch_pdl(k_mix, dim3(B), dim3(1024), 0, s, Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(kMixCl, B);
+  lc.blockDim = dim3(kMixThreads);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kMixCl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  cudaLaunchKernelEx(&lc, k_mix, (const float*)Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
 }
 
 // ------------------------------------------------------------------ MoE (router replay)
 // Router logits r[m][e] = Wr[e] · un[m] with the normed row unrounded (fp32)
-// and Wr stored in the weight type: one CTA per stacked row holds the row in
-// shared memory; warp w computes experts w, w+8, ... with 16-byte weight loads.
-template <typename TW>
-__global__ void k_router(const TW* __restrict__ Wr, const float* __restrict__ un, float* __restrict__ rlog, int E,
-                         int d, int lo) {
+// and Wr stored in the weight type.  CTA (row block, expert block): up to
+// kRouterRows consecutive stacked rows held in shared memory, warp w computes
+// expert 8*blockIdx.y + w for all of them with 16-byte weight loads (each
+// weight vector is read once per row block).
+template <typename TW, int R>
+__global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const float* __restrict__ un,
+                                                float* __restrict__ rlog, int E, int d, int lo, int hi) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  extern __shared__ float xrow[];
-  const int m = lo + blockIdx.x;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) xrow[i] = un[(size_t)m * d + i];
+  extern __shared__ float xrows[];  // [R][d]
+  const int m0 = lo + blockIdx.x * R;
+  const int nr = min(R, hi - m0);
+  for (int i = threadIdx.x; i < nr * d; i += blockDim.x) xrows[i] = un[(size_t)m0 * d + i];
   __syncthreads();
-  const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.y * 8 + w;
+  if (e >= E) return;
   constexpr int VEC = 16 / sizeof(TW);
-  for (int e = w; e < E; e += warps) {
-    const TW* wr = Wr + (size_t)e * d;
-    float acc = 0.f;
-    for (int k0 = lane * VEC; k0 < d; k0 += 32 * VEC) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(wr + k0);
-      const TW* wv = reinterpret_cast<const TW*>(&raw);
+  const TW* wr = Wr + (size_t)e * d;
+  float acc[R];
 #pragma unroll
-      for (int q = 0; q < VEC; ++q) acc = fmaf(Num<TW>::to_f(wv[q]), xrow[k0 + q], acc);
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  for (int k0 = lane * VEC; k0 < d; k0 += 32 * VEC) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(wr + k0);
+    const TW* wv = reinterpret_cast<const TW*>(&raw);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r >= nr) break;
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) acc[r] = fmaf(Num<TW>::to_f(wv[q]), xrows[r * d + k0 + q], acc[r]);
     }
-    acc = warp_sum(acc);
-    if (lane == 0) rlog[(size_t)m * E + e] = acc;
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (r >= nr) break;
+    const float v = warp_sum(acc[r]);
+    if (lane == 0) rlog[(size_t)(m0 + r) * E + e] = v;
   }
 }
 
 void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s) {
   const int n = R.hi - R.lo;
   if (n <= 0) return;
-  const size_t smem = (size_t)D.d * sizeof(float);
+  const dim3 grid((n + kRouterRows - 1) / kRouterRows, (D.E + 7) / 8);
+  const size_t smem = (size_t)kRouterRows * D.d * sizeof(float);  // d <= 8192: at most 128 KB
   if (D.bf16)
-    launch_pdl(k_router<__nv_bfloat16>, dim3(n), dim3(256), smem, s, (const __nv_bfloat16*)Wr, (const float*)Bf.un,
-               Bf.rlog, D.E, D.d, R.lo);
+    launch_pdl(k_router<__nv_bfloat16, kRouterRows>, grid, dim3(256), smem, s, (const __nv_bfloat16*)Wr,
+               (const float*)Bf.un, Bf.rlog, D.E, D.d, R.lo, R.hi);
   else
-    launch_pdl(k_router<float>, dim3(n), dim3(256), smem, s, (const float*)Wr, (const float*)Bf.un, Bf.rlog, D.E,
-               D.d, R.lo);
+    launch_pdl(k_router<float, kRouterRows>, grid, dim3(256), smem, s, (const float*)Wr, (const float*)Bf.un,
+               Bf.rlog, D.E, D.d, R.lo, R.hi);
 }
 
 // The primary rows choose their top-k experts (descending router logit,
@@ -699,6 +802,7 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
   // one warp per primary row: k rounds of a warp-wide argmax (larger value
   // wins, equal values -> lower index) over the experts not yet taken
   for (int b = w; b < B; b += warps) {
+    int sel = 0;  // lane j < k: the j-th selected expert
     if (select) {
       const float* r = rlog + (size_t)b * E;
       unsigned long long taken_lo = 0ull, taken_hi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
@@ -725,6 +829,7 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
           }
         }
         if (lane == 0) topk_l[b * k + j] = bi;
+        if (lane == j) sel = bi;
         if (bi != 0x7fffffff && (bi % 32) == lane) {
           const int qq = bi / 32;
           if (qq < 64)
@@ -733,33 +838,41 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
             taken_hi |= 1ull << (qq - 64);
         }
       }
+    } else if (lane < k) {
+      sel = topk_l[b * k + lane];
     }
-    __syncwarp();
-    if (lane == 0) {
-      for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
-        const float* r = rlog + (size_t)(f * B + b) * E;
-        float mx = -INFINITY;
-        for (int j = 0; j < k; ++j) mx = fmaxf(mx, r[topk_l[b * k + j]]);
-        float den = 0.f;
-        for (int j = 0; j < k; ++j) den += expf(r[topk_l[b * k + j]] - mx);
-        for (int j = 0; j < k; ++j) gate[(size_t)(f * B + b) * k + j] = expf(r[topk_l[b * k + j]] - mx) / den;
-      }
-      if (dbg_topk_l && prim)
-        for (int j = 0; j < k; ++j) dbg_topk_l[b * k + j] = topk_l[b * k + j];
+    // gates: lane j holds entry j; max and sum taken in entry order
+    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+      const float* r = rlog + (size_t)(f * B + b) * E;
+      const float v = lane < k ? r[sel] : -INFINITY;
+      float mx = -INFINITY;
+      for (int j = 0; j < k; ++j) mx = fmaxf(mx, __shfl_sync(0xffffffffu, v, j));
+      const float ex = lane < k ? expf(v - mx) : 0.f;
+      float den = 0.f;
+      for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
+      if (lane < k) gate[(size_t)(f * B + b) * k + lane] = ex / den;
     }
+    if (dbg_topk_l && prim && lane < k) dbg_topk_l[b * k + lane] = sel;
     if (dbg_router_l && prim)
       for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  // entry lists in ascending entry order: warp per expert, 32 entries a round
+  const int nent = B * k;
+  for (int e = w; e < E; e += warps) {
     int cnt = 0;
-    for (int b = 0; b < B; ++b)
-      for (int j = 0; j < k; ++j)
-        if (topk_l[b * k + j] == e) {
-          eslot[b * k + j] = cnt;
-          elist[(size_t)e * maxB + cnt++] = b * k + j;
-        }
-    ecount[e] = cnt;
+    for (int base = 0; base < nent; base += 32) {
+      const int idx = base + lane;
+      const bool hit = idx < nent && topk_l[idx] == e;
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (hit) {
+        const int slot = cnt + __popc(m & ((1u << lane) - 1u));
+        eslot[idx] = slot;
+        elist[(size_t)e * maxB + slot] = idx;
+      }
+      cnt += __popc(m);
+    }
+    if (lane == 0) ecount[e] = cnt;
   }
 }
 

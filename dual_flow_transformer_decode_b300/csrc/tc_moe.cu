@@ -201,38 +201,44 @@ __global__ void k_moe_gather(const __nv_bfloat16* __restrict__ u, const int* __r
 }
 
 // y_f = sum_j gate_f[j] * y_expert(e_j)[row of (b, j, f)] in slot order,
-// y2 += c ⊙ y1, h += y.
+// y2 += c ⊙ y1, h += y.  CTA (stacked row, 256-feature chunk); the row's
+// entries (expert, output row, gates) are staged in shared memory first.
+constexpr int kCombineMaxK = 16;
+
 __global__ void k_moe_combine_tc(const float* __restrict__ yE, const float* __restrict__ gate,
                                  const int* __restrict__ topk_l, const int* __restrict__ eslot,
                                  const float* __restrict__ cvec, float* __restrict__ h, Couple C, int B, int lo,
                                  int d, int k, int nxe) {
+  __shared__ size_t ofs[kCombineMaxK];  // start of the primary row of entry j in yE
+  __shared__ float g_own[kCombineMaxK], g_prim[kCombineMaxK];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int m = lo + blockIdx.x;
   const int f = m >= B, b = m - f * B;
-  for (int n = threadIdx.x; n < d; n += blockDim.x) {
-    float y = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int e = topk_l[b * k + j], row = 2 * eslot[b * k + j] + f;
-      y = fmaf(gate[(size_t)m * k + j], yE[((size_t)e * nxe + row) * d + n], y);
-    }
-    if (f) {
-      float y1;
-      if (C.saved) {
-        y1 = C.y1s[(size_t)b * d + n];
-      } else {
-        y1 = 0.f;
-        for (int j = 0; j < k; ++j) {
-          const int e = topk_l[b * k + j], row = 2 * eslot[b * k + j];
-          y1 = fmaf(gate[(size_t)b * k + j], yE[((size_t)e * nxe + row) * d + n], y1);
-        }
-      }
-      y = fmaf(cvec[n], y1, y);
-    } else if (C.save) {
-      C.y1s[(size_t)b * d + n] = y;
-    }
-    h[(size_t)m * d + n] += y;
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    ofs[j] = ((size_t)topk_l[b * k + j] * nxe + 2 * eslot[b * k + j]) * d;
+    g_own[j] = gate[(size_t)m * k + j];
+    g_prim[j] = gate[(size_t)b * k + j];
   }
+  __syncthreads();
+  const int n = blockIdx.y * blockDim.x + threadIdx.x;
+  if (n >= d) return;
+  float y = 0.f;
+  for (int j = 0; j < k; ++j) y = fmaf(g_own[j], yE[ofs[j] + (size_t)f * d + n], y);
+  if (f) {
+    float y1;
+    if (C.saved) {
+      y1 = C.y1s[(size_t)b * d + n];
+    } else {
+      y1 = 0.f;
+      for (int j = 0; j < k; ++j) y1 = fmaf(g_prim[j], yE[ofs[j] + n], y1);
+    }
+    y = fmaf(cvec[n], y1, y);
+  } else if (C.save) {
+    C.y1s[(size_t)b * d + n] = y;
+  }
+  h[(size_t)m * d + n] += y;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -329,7 +335,7 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
   a.rows_w = D.d;
   launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe), s, P.w_d[layer], P.x_z, D.Fe, a);
   const int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo), dim3(256), 0, s, (const float*)Bf.yEt, (const float*)Bf.gate,
+  launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt, (const float*)Bf.gate,
              topk_l, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, P.nxe);
 }
 
