@@ -253,6 +253,22 @@ def run_ours(args, rank, world, local_rank):
         return {"metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
                 "quick": True, "config": {"workload": cfg.name}, "kernels_per_step": kernels, "clocks": clk}
 
+    # per-step latency distribution: an event pair around every step
+    model.set_length(B, P)
+    for s in range(min(W, 3)):
+        step(s)
+    n_lat = min(K, 64)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_lat + 1)]
+    torch.cuda.synchronize(dev)
+    evs[0].record(stream)
+    for i in range(n_lat):
+        step(min(W, 3) + i)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    lat = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(n_lat))
+    latency = {"steps": n_lat, "p50_ms": round(lat[len(lat) // 2], 4),
+               "p90_ms": round(lat[min(len(lat) - 1, (9 * len(lat)) // 10)], 4), "max_ms": round(lat[-1], 4)}
+
     # ablations on the same positions: two ungrouped passes, and primary-only decode
     abl = {}
     for name, aux, ung in (("ungrouped_two_pass", 1, 1), ("aux_off_standard_decode", 0, 0)):
@@ -260,7 +276,9 @@ def run_ours(args, rank, world, local_rank):
         model.set_mode(aux, ung)
         kk = min(K, 32)
         ms = max_over_ranks(timed(min(W, 3), kk)) / kk
-        abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1)}
+        abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1),
+                     # two passes each read every weight and the whole cache; primary-only reads them once
+                     "algorithmic_bytes": 2 * step_bytes(cfg, B, t_mid) if ung else step_bytes(cfg, B, t_mid)}
     model.set_mode(1, 0)
 
     # dominant operation: time every op, cycling layers, with CUDA events
@@ -315,6 +333,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac_of_measured": round(step_gbs / hbm_peak, 4), "frac_of_8tbs": round(step_gbs / 8000, 4)},
         "roofline": roofline,
         "ops_ms_per_launch": {o: round(v, 5) for o, v in op_ms.items()},
+        "step_latency": latency,
         "ablation": abl,
         "e2e": e2e,
         "gpu_launches": kernels * K if kernels >= 0 else None,

@@ -47,7 +47,7 @@ EXPORTS = ["df_workspace_bytes", "df_create", "df_prefill", "df_set_length", "df
            "df_decode_step_host", "df_set_mode", "df_debug_outputs", "df_sync", "df_length",
            "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc"]
 
-DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6}
+DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6, "layers": 7}
 
 
 def lib():

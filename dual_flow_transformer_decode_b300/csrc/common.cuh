@@ -15,7 +15,8 @@ struct Ctrl {
   int t;          // current position (number of valid cache positions)
   int err;        // first latched device error (0 = none)
   int err_info;   // kernel-specific detail for the first error
-  int pad[61];
+  int mk_abort;   // set by a persistent-kernel CTA that gave up; the others stop waiting
+  int pad[60];
 };
 
 __device__ __forceinline__ void latch_error(Ctrl* c, int code, int info) {

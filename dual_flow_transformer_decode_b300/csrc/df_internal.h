@@ -82,6 +82,8 @@ struct Buffers {
   size_t tickets_cap;
   float* gpart;     // split-K partial tiles
   size_t gpart_cap; // floats
+  void* mk;         // persistent-kernel region (maps, task lists, counters, partials)
+  size_t mk_bytes;
 };
 
 // Which rows of the stacked block a launch works on.

@@ -28,6 +28,7 @@
 #include "tc_gemm.h"
 #include "tc_moe.h"
 #include "attn_fast.h"
+#include "mk_step.h"
 
 using df::Buffers;
 using df::Couple;
@@ -85,6 +86,7 @@ struct df_ctx {
   df::TcPlan tc;
   df::MoePlan moe;
   df::AttnPlan at;
+  df::MkPlan mk;
   std::string err;
 };
 
@@ -216,6 +218,8 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.attn_tickets = (int*)take((size_t)D.maxB * D.Hkv * 4);
   b.gpart_cap = df::tc_partial_floats(D);
   b.gpart = (float*)take(b.gpart_cap * 4);
+  b.mk_bytes = df::mk_workspace_bytes(D);
+  b.mk = b.mk_bytes ? take(b.mk_bytes) : nullptr;
   if (Bf) *Bf = b;
   return cur;
 }
@@ -326,10 +330,16 @@ void op_lm(df_ctx* X, const Rows& R) {
   }
 }
 
-void enqueue_pass(df_ctx* X, const Rows& R, int save, int saved, bool lm) {
+// Every layer of a pass over rows R: one persistent-kernel launch where it
+// applies, else the kernel sequence per layer.
+void enqueue_layers(df_ctx* X, const Rows& R, int save, int saved) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
+  if (!X->force_generic && df::mk_can_run(X->mk, R)) {
+    df::mk_launch(X->mk, D, Bf, X->kv, R, save, saved, s);
+    return;
+  }
   for (int l = 0; l < D.L; ++l) {
     Couple C = layer_couple(X, l, save, saved);
     df::launch_rmsnorm(D, Bf, X->attn_norm[l], Bf.u, nullptr, R, s);
@@ -344,6 +354,13 @@ void enqueue_pass(df_ctx* X, const Rows& R, int save, int saved, bool lm) {
       op_down(X, l, R, C);
     }
   }
+}
+
+void enqueue_pass(df_ctx* X, const Rows& R, int save, int saved, bool lm) {
+  const Dims& D = X->D;
+  const Buffers& Bf = X->Bf;
+  cudaStream_t s = X->stream;
+  enqueue_layers(X, R, save, saved);
   if (lm) {
     df::launch_rmsnorm(D, Bf, X->final_norm, Bf.u, nullptr, R, s);
     op_lm(X, R);
@@ -524,7 +541,9 @@ df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, voi
   std::string perr;
   if (!df::tc_plan_init(X->tc, X->D, X->Bf, X->wqkv, X->wo, X->wgu, X->wd, X->lm_head, &perr) ||
       (X->D.E && !df::moe_tc_init(X->moe, X->D, X->Bf, X->wgu, X->wd, &perr)) ||
-      !df::attn_fast_init(X->at, X->D, X->kv, &perr)) {
+      !df::attn_fast_init(X->at, X->D, X->kv, &perr) ||
+      !df::mk_init(X->mk, X->D, X->Bf, X->Bf.mk, X->kv, X->wqkv, X->wo, X->wgu, X->wd, X->attn_norm, X->mlp_norm,
+                   X->a, X->b, X->c, X->stream, &perr)) {
     fprintf(stderr, "df_create: %s\n", perr.c_str());
     if (X->own_stream) cudaStreamDestroy(X->stream);
     delete X;
@@ -543,6 +562,7 @@ static df_status set_batch(df_ctx* X, int B) {
     X->splits = df::attn_splits(X->D, B);
     std::string perr;
     if (!df::tc_plan_batch(X->tc, X->D, B, &perr)) return fail(X, DF_ERR_CUDA, perr);
+    if (!df::mk_batch(X->mk, X->D, X->Bf, B, &perr)) return fail(X, DF_ERR_CUDA, perr);
   }
   return DF_OK;
 }
@@ -611,12 +631,16 @@ df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int3
 df_status df_sync(df_ctx* X) {
   if (!X) return DF_ERR_ARG;
   df::Ctrl h{};
-  cudaError_t e = cudaMemcpyAsync(&h, X->Bf.ctrl, sizeof(int) * 4, cudaMemcpyDeviceToHost, X->stream);
+  cudaError_t e = cudaMemcpyAsync(&h, X->Bf.ctrl, sizeof(h), cudaMemcpyDeviceToHost, X->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(X->stream);
   if (e != cudaSuccess) return cuda_fail(X, e, "df_sync");
   if (h.err) {
-    char buf[128];
-    snprintf(buf, sizeof(buf), "device error %d (detail %d)", h.err, h.err_info);
+    char buf[256];
+    if (h.err_info >= 300 && h.err_info < 400)  // persistent kernel: where it gave up
+      snprintf(buf, sizeof(buf), "device error %d (detail %d: cta %d, awaited %d, target %d, seen %d, thread %d)",
+               h.err, h.err_info, h.pad[0], h.pad[1], h.pad[2], h.pad[3], h.pad[4]);
+    else
+      snprintf(buf, sizeof(buf), "device error %d (detail %d)", h.err, h.err_info);
     X->err = buf;
     // the error is reported once; clear the latch so the context stays usable
     cudaMemsetAsync(&X->Bf.ctrl->err, 0, 2 * sizeof(int), X->stream);
@@ -666,7 +690,7 @@ df_status df_debug_outputs(df_ctx* X, float* logp1, float* logp2, int32_t* topk,
 df_status df_time_op(df_ctx* X, int op, int iters, float* avg_ms) {
   if (!X || !avg_ms || iters <= 0) return DF_ERR_ARG;
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_time_op before df_prefill");
-  if (op < 0 || op > DF_OP_MOE) return fail(X, DF_ERR_ARG, "df_time_op: unknown op");
+  if (op < 0 || op > DF_OP_LAYERS) return fail(X, DF_ERR_ARG, "df_time_op: unknown op");
   if (op == DF_OP_MOE && !X->D.E) return fail(X, DF_ERR_ARG, "df_time_op: MoE op on a dense model");
   if ((op == DF_OP_GATEUP || op == DF_OP_DOWN) && X->D.E) return fail(X, DF_ERR_ARG, "df_time_op: dense op on MoE");
   int B = X->B;
@@ -686,6 +710,7 @@ df_status df_time_op(df_ctx* X, int op, int iters, float* avg_ms) {
       case DF_OP_DOWN: op_down(X, l, R, C); break;
       case DF_OP_LMHEAD: op_lm(X, R); break;
       case DF_OP_MOE: op_moe(X, l, R, C); break;
+      case DF_OP_LAYERS: enqueue_layers(X, R, 0, 0); break;
     }
   }
   cudaEventRecord(e1, X->stream);
@@ -794,12 +819,17 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
   key.i[3] = X->force_generic;
   key.i[4] = X->dbg_router != nullptr;
   StepOut o{logp_mix, argmax, alpha};
-  // The step is enqueued with the partials pointed at the static array.
+  // The step is enqueued with the partials pointed at the static array (the
+  // split-attention partials of the kernel sequence, or those of the
+  // persistent kernel, whichever path the step takes).
   Buffers saved = X->Bf;
+  float* saved_apart = X->mk.apart;
   X->Bf.part_o = scratch;
   X->Bf.part_ml = scratch + parts * X->D.hd;
+  X->mk.apart = scratch;
   df_status st = run_captured(X, X->dec_static, key, [&] { enqueue_decode(X, tokens, o); }, 1);
   X->Bf = saved;
+  X->mk.apart = saved_apart;
   if (st != DF_OK) return st;
   X->t += 1;
   return DF_OK;

@@ -207,7 +207,12 @@ enum {
   DF_OP_GATEUP = 3,  /* gate/up projection + SwiGLU + b coupling (dense)     */
   DF_OP_DOWN = 4,    /* down projection + c coupling + residual (dense)      */
   DF_OP_LMHEAD = 5,  /* LM head                                              */
-  DF_OP_MOE = 6      /* router + replayed experts + combine (MoE)            */
+  DF_OP_MOE = 6,     /* router + replayed experts + combine (MoE)            */
+  DF_OP_LAYERS = 7   /* every layer of a grouped pass: the per-layer kernel
+                        sequence, or one persistent-kernel launch where that
+                        is enabled (DF_MK=1) and applies (dense bf16,
+                        head_dim 128, at most 32 stacked rows); iterations
+                        are whole passes, not layers                        */
 };
 df_status df_time_op(df_ctx* ctx, int op, int iters, float* avg_ms);
 

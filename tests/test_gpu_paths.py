@@ -38,3 +38,39 @@ def test_fast_path_matches_cuda_core_path(name, cuda_device):
     assert diff.max() < 0.05 and rel < 2.0 ** -8
     fast.close()
     ref.close()
+
+
+@pytest.mark.parametrize("name,aux,ungrouped", [("t_bf16", True, False), ("t_bf16_b9", True, False),
+                                                ("t_bf16_long", True, False), ("t_bf16", False, False),
+                                                ("t_bf16", True, True)])
+def test_persistent_kernel_matches_kernel_sequence(name, aux, ungrouped, cuda_device):
+    """The one-launch persistent pass (opt-in with DF_MK=1; dense bf16, up to
+    32 stacked rows) against the per-layer kernel sequence of the same
+    library: prefill and decode, both flows, aux-off and the two-pass
+    ungrouped mode."""
+    cfg = dfsynth.get_config(name).with_(n_steps=3)
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    ref = GpuRun(cfg, w, tok, aux=aux, ungrouped=ungrouped)
+    os.environ["DF_MK"] = "1"
+    try:
+        mk = GpuRun(cfg, w, tok, aux=aux, ungrouped=ungrouped)
+    finally:
+        del os.environ["DF_MK"]
+    # one launch for all layers of a pass instead of seven per layer
+    print("kernels per step", mk.m.step_kernels, ref.m.step_kernels)
+    assert 0 < mk.m.step_kernels < ref.m.step_kernels
+    for a, b in zip(mk.steps, ref.steps):
+        d1 = np.abs(a["logp1"] - b["logp1"]).max()
+        dm = np.abs(a["logp_mix"] - b["logp_mix"]).max()
+        print(name, aux, ungrouped, "max |dlogp1|", d1, "max |dlogp_mix|", dm)
+        assert d1 < 5e-3 and dm < 5e-3
+        if aux:
+            d2 = np.abs(a["logp2"] - b["logp2"]).max()
+            assert d2 < 5e-3, d2
+    diff = np.abs(mk.kv - ref.kv).astype(np.float64)
+    rel = float(np.sqrt((diff ** 2).sum() / (ref.kv.astype(np.float64) ** 2).sum()))
+    print("kv max", diff.max(), "relative rms", rel)
+    assert diff.max() < 0.05 and rel < 2.0 ** -8
+    mk.close()
+    ref.close()
