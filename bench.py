@@ -253,6 +253,19 @@ def run_ours(args, rank, world, local_rank):
         return {"metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
                 "quick": True, "config": {"workload": cfg.name}, "kernels_per_step": kernels, "clocks": clk}
 
+    # MoE: the experts a step actually reads, per layer (union of the primary
+    # top-k sets over the batch), from the routing of one step at t_mid
+    moe_union = None
+    if cfg.n_experts:
+        tk = torch.zeros(cfg.n_layers, B, cfg.top_k, dtype=torch.int32, device=dev)
+        model.debug_outputs(topk=tk)
+        model.set_length(B, t_mid)
+        step(0)
+        model.sync()
+        tkh = tk.cpu().numpy()
+        moe_union = float(np.mean([len(np.unique(tkh[l])) for l in range(cfg.n_layers)]))
+        model.debug_outputs()
+
     # per-step latency distribution: an event pair around every step
     model.set_length(B, P)
     for s in range(min(W, 3)):
@@ -278,7 +291,8 @@ def run_ours(args, rank, world, local_rank):
         ms = max_over_ranks(timed(min(W, 3), kk)) / kk
         abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1),
                      # two passes each read every weight and the whole cache; primary-only reads them once
-                     "algorithmic_bytes": 2 * step_bytes(cfg, B, t_mid) if ung else step_bytes(cfg, B, t_mid)}
+                     "algorithmic_bytes": 2 * step_bytes(cfg, B, t_mid, moe_union) if ung
+                     else step_bytes(cfg, B, t_mid, moe_union)}
     model.set_mode(1, 0)
 
     # dominant operation: time every op, cycling layers, with CUDA events
@@ -293,13 +307,13 @@ def run_ours(args, rank, world, local_rank):
     shares = {o: op_ms[o] * per_step_count[o] for o in ops}
     dom = max(shares, key=shares.get)
     hbm_peak, _, peak_kind = _peaks()
-    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mid + 1)
+    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mid + 1, moe_union)
     achieved = bytes_dom / (op_ms[dom] / 1e3) / 1e9
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": captured_traffic(cfg.name, dom),
                 "peak_source": peak_kind, "ms_per_launch": round(op_ms[dom], 5),
                 "algorithmic_bytes_per_launch": bytes_dom}
-    sb = step_bytes(cfg, B, t_mid)
+    sb = step_bytes(cfg, B, t_mid, moe_union)
     step_gbs = sb / (ms_step / 1e3) / 1e9
 
     # end to end through the host-buffer entry point (pinned host memory)
@@ -334,6 +348,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "ops_ms_per_launch": {o: round(v, 5) for o, v in op_ms.items()},
         "step_latency": latency,
+        "moe_experts_read_per_layer": moe_union,
         "ablation": abl,
         "e2e": e2e,
         "gpu_launches": kernels * K if kernels >= 0 else None,
