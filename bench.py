@@ -42,6 +42,14 @@ def _peaks():
         return 6400.0, 1800.0, "fallback"
 
 
+def _bf16_sustained():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1400.0
+
+
 class Clocks:
     """nvidia-smi sampler for the timed region."""
 
@@ -157,6 +165,17 @@ def algorithmic_bytes(cfg, op: str, B: int, t: int, moe_union: float | None = No
     raise KeyError(op)
 
 
+def prefill_flops(cfg, B: int, P: int) -> float:
+    """Multiply-add flops of prefilling P positions of B sequences through the
+    primary flow: every weight matrix of every layer on each of the B*P rows,
+    plus causal attention (scores and weighted values over positions <= p)."""
+    d, qd, kvd = cfg.d_model, cfg.q_dim, cfg.kv_dim
+    mlp = 3 * cfg.ffn_hidden * d if not cfg.n_experts else 3 * cfg.top_k * cfg.expert_hidden * d
+    per_row = (qd + 2 * kvd) * d + d * qd + mlp
+    attn = 4.0 * B * cfg.n_heads * cfg.head_dim * (P * (P + 1) / 2)
+    return cfg.n_layers * (2.0 * B * P * per_row + attn)
+
+
 def step_bytes(cfg, B: int, t: int, moe_union: float | None = None) -> float:
     L = cfg.n_layers
     per_layer = algorithmic_bytes(cfg, "qkv", B, t) + algorithmic_bytes(cfg, "attn", B, t) + \
@@ -193,10 +212,29 @@ def run_ours(args, rank, world, local_rank):
     model = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, args.seed, dev), max_batch=B, max_len=max_len,
                           device=dev)
     tok_d = torch.from_numpy(tok).to(dev)
+    prefill = None
     if args.quick:
         model.set_length(B, P)   # timing-only: cache contents do not change the work
     else:
-        model.prefill(tok_d[:, :P].contiguous())
+        # prefill of the prompt (primary flow only), timed once with CUDA events
+        prompt = tok_d[:, :P].contiguous()
+        model.sync()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(model.stream)
+        model.prefill(prompt)
+        p1.record(model.stream)
+        model.sync()
+        pms = p0.elapsed_time(p1)
+        flop = prefill_flops(cfg, B, P)
+        bf16_peak = _bf16_sustained()  # the prefill runs for tens of milliseconds
+        prefill = {"positions": P, "batch": B, "ms": round(pms, 3), "tokens_per_s": round(B * P / (pms / 1e3), 1),
+                   "algorithmic_tflop": round(flop / 1e12, 3),
+                   "achieved_tflops": round(flop / (pms / 1e3) / 1e12, 1),
+                   "peak_tflops": bf16_peak, "peak_kind": "measured bf16 sustained",
+                   "frac_of_bf16_peak": round(flop / (pms / 1e3) / 1e12 / bf16_peak, 4),
+                   "path": "serial" if os.environ.get("DF_SERIAL_PREFILL") == "1" or cfg.n_experts or
+                   cfg.dtype != "bf16" else "batched"}
     model.sync()
     steps_tok = tok_d[:, P:].t().contiguous()          # [span][B]
     # The step graph is cached per (token buffer, output buffers): feed each
@@ -348,6 +386,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "ops_ms_per_launch": {o: round(v, 5) for o, v in op_ms.items()},
         "step_latency": latency,
+        "prefill": prefill,
         "moe_experts_read_per_layer": moe_union,
         "ablation": abl,
         "e2e": e2e,

@@ -84,6 +84,8 @@ struct Buffers {
   size_t gpart_cap; // floats
   void* mk;         // persistent-kernel region (maps, task lists, counters, partials)
   size_t mk_bytes;
+  void* bp;         // batched-prefill chunk buffers
+  size_t bp_bytes;
 };
 
 // Which rows of the stacked block a launch works on.
@@ -113,6 +115,8 @@ void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void
                   const int32_t* tokens, int tok_stride, int use_pos, const Rows& R, cudaStream_t s);
 void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out, float* out_f32,
                     const Rows& R, cudaStream_t s);
+// RMSNorm of rows 0..rows-1 of h (row stride d) into out (storage type).
+void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s);
 
 // CUDA-core GEMV: out[m][n] = sum_k W[n][k] X[m][k] for rows m in [lo, hi).
 // x_f32: X is fp32 (router) instead of dtype.

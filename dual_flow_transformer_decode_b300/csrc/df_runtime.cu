@@ -29,6 +29,7 @@
 #include "tc_moe.h"
 #include "attn_fast.h"
 #include "mk_step.h"
+#include "prefill.h"
 
 using df::Buffers;
 using df::Couple;
@@ -87,6 +88,7 @@ struct df_ctx {
   df::MoePlan moe;
   df::AttnPlan at;
   df::MkPlan mk;
+  df::BpPlan bp;
   std::string err;
 };
 
@@ -220,6 +222,8 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.gpart = (float*)take(b.gpart_cap * 4);
   b.mk_bytes = df::mk_workspace_bytes(D);
   b.mk = b.mk_bytes ? take(b.mk_bytes) : nullptr;
+  b.bp_bytes = df::bp_workspace_bytes(D);
+  b.bp = b.bp_bytes ? take(b.bp_bytes) : nullptr;
   if (Bf) *Bf = b;
   return cur;
 }
@@ -543,7 +547,8 @@ df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, voi
       (X->D.E && !df::moe_tc_init(X->moe, X->D, X->Bf, X->wgu, X->wd, &perr)) ||
       !df::attn_fast_init(X->at, X->D, X->kv, &perr) ||
       !df::mk_init(X->mk, X->D, X->Bf, X->Bf.mk, X->kv, X->wqkv, X->wo, X->wgu, X->wd, X->attn_norm, X->mlp_norm,
-                   X->a, X->b, X->c, X->stream, &perr)) {
+                   X->a, X->b, X->c, X->stream, &perr) ||
+      !df::bp_init(X->bp, X->D, X->Bf.bp, &perr)) {
     fprintf(stderr, "df_create: %s\n", perr.c_str());
     if (X->own_stream) cudaStreamDestroy(X->stream);
     delete X;
@@ -578,6 +583,17 @@ df_status df_prefill(df_ctx* X, const int32_t* tokens, int B, int n) {
   X->t = 0;
   X->ready = true;
   if (n == 0) return DF_OK;
+  if (X->bp.enabled && X->tc.enabled && X->at.enabled && !X->force_generic) {
+    // batched: every layer once per chunk of positions (kernels enqueued directly)
+    df::bp_prefill(X->bp, X->tc, X->at, X->D, X->Bf, X->kv, X->emb1, X->attn_norm.data(), X->mlp_norm.data(),
+                   tokens, B, n, X->stream);
+    df::launch_set_pos(X->Bf.ctrl, n, X->stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(X, e, "batched prefill launch");
+    X->last_kernels = -1;
+    X->t = n;
+    return DF_OK;
+  }
   GraphKey key{};
   key.p[0] = tokens;
   key.i[0] = n;

@@ -161,6 +161,15 @@ void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out,
     launch_pdl(k_rmsnorm<float>, dim3(n), dim3(256), 0, s, Bf.h, g, (float*)out, out_f32, D.d, D.eps, R.lo);
 }
 
+void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s) {
+  if (rows <= 0) return;
+  if (D.bf16)
+    launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, h, g, (__nv_bfloat16*)out, (float*)nullptr,
+               D.d, D.eps, 0);
+  else
+    launch_pdl(k_rmsnorm<float>, dim3(rows), dim3(256), 0, s, h, g, (float*)out, (float*)nullptr, D.d, D.eps, 0);
+}
+
 // ------------------------------------------------------------------ GEMV (CUDA cores)
 // One warp per output feature; lanes stride the reduction dimension with
 // coalesced loads; rows are processed R at a time with one accumulator each.

@@ -1,0 +1,40 @@
+// Batched (chunked) prefill for dense bf16 models with head_dim 128.
+#pragma once
+
+#include <cuda.h>
+
+#include <string>
+
+#include "df_internal.h"
+
+namespace df {
+
+struct TcPlan;
+struct AttnPlan;
+
+struct BpPlan {
+  bool enabled = false;
+  int mcap = 0;                 // activation rows per chunk (B x positions), a multiple of 128
+  float* h = nullptr;           // [mcap][d] residual rows of the chunk
+  void* u = nullptr;            // [mcap][d] normed rows (bf16)
+  void* q = nullptr;            // [mcap][qdim] rotated queries (bf16)
+  void* o = nullptr;            // [mcap][qdim] attention output (bf16)
+  void* z = nullptr;            // [mcap][F] SwiGLU output (bf16)
+  CUtensorMap x_u, x_o, x_z;    // activation maps, 128-row boxes
+};
+
+// Rows per chunk for a model, or 0 when batched prefill does not apply
+// (bf16, dense, head_dim 128, 128-multiple widths).
+int bp_rows(const Dims& D);
+// Workspace bytes of the chunk buffers (0 when it does not apply).
+size_t bp_workspace_bytes(const Dims& D);
+// Carves the chunk buffers from `region` and encodes their tensor maps.
+bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err);
+// Prefill positions [0, n) of B sequences (primary flow only): tokens is a
+// device [B][n] array of ids.  Every layer runs once per chunk of positions;
+// the KV cache receives positions 0..n-1.  Enqueued on `s`.
+void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dims& D, const Buffers& Bf,
+                void* kv, const void* emb1, const float* const* attn_norm, const float* const* mlp_norm,
+                const int32_t* tokens, int B, int n, cudaStream_t s);
+
+}  // namespace df

@@ -41,7 +41,10 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
+#ifndef DF_GEMM_WIDE_KB
+#define DF_GEMM_WIDE_KB 96
+#endif
 constexpr int kBK = 64;                 // K elements per stage (one 128-byte swizzle atom of bf16)
 constexpr int kBM = 128;                // weight rows per tile (MMA M)
 constexpr int kStageW = kBM * kBK * 2;  // 16 KB
@@ -432,17 +435,16 @@ int choose_splits(int n_out, int K, int sms, int per_sm) {
   return s;
 }
 
-// Ring depth: as many stages as fit in ~64 KB (at least 2), so that two GEMM
-// CTAs and a CTA of the neighbouring kernel fit on one SM.
-int stages_for(int N) {
-  int st = (64 * 1024) / (kStageW + N * kBK * 2);
+// Ring depth: as many stages as fit in `kb` KB (at least 2).
+int stages_for(int N, int kb = 64) {
+  int st = (kb * 1024) / (kStageW + N * kBK * 2);
   if (st > kMaxStages) st = kMaxStages;
   if (st < 2) st = 2;
   return st;
 }
 
-size_t smem_bytes(int N) {
-  size_t region = (size_t)stages_for(N) * (kStageW + N * kBK * 2);
+size_t smem_bytes(int N, int stages) {
+  size_t region = (size_t)stages * (kStageW + N * kBK * 2);
   if ((size_t)N * kBM * 4 > region) region = (size_t)N * kBM * 4;  // epilogue partial tile
   return region + 1024 + 4 * 64 * 4 + 256;
 }
@@ -505,7 +507,8 @@ bool tc_plan_batch(TcPlan& P, const Dims& D, int B, std::string* err) {
   int N = (2 * B + 15) / 16 * 16;
   P.npad = N;
   // the split plan depends on how many CTAs of this N fit on one SM
-  const int per_sm = (int)((227 * 1024) / (smem_bytes(N) + 1024));
+  P.sms = D.sms;
+  const int per_sm = (int)((227 * 1024) / (smem_bytes(N, stages_for(N)) + 1024));
   P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms, per_sm);
   P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms, per_sm);
   P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms, per_sm);
@@ -562,7 +565,11 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(tiles_of(n_out) * splits);
   lc.blockDim = dim3(128);
-  lc.dynamicSmemBytes = smem_bytes(P.npad);
+  // ~64 KB rings let two GEMM CTAs and a neighbouring kernel's CTA share an
+  // SM; a launch of at most one CTA per SM may use a deeper ring.
+  const bool one_per_sm = tiles_of(n_out) * splits <= P.sms;
+  const int stages = stages_for(P.npad, one_per_sm ? DF_GEMM_WIDE_KB : 64);
+  lc.dynamicSmemBytes = smem_bytes(P.npad, stages);
   lc.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -573,7 +580,7 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n
   at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   lc.attrs = at;
   lc.numAttrs = 2;
-  cudaLaunchKernelEx(&lc, k_tc_gemm, tw, tx, P.npad, K / kBK, stages_for(P.npad), ep, Bf.ctrl);
+  cudaLaunchKernelEx(&lc, k_tc_gemm, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
 }
 
 }  // namespace

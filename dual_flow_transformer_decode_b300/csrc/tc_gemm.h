@@ -15,6 +15,7 @@ struct TcPlan {
   bool enabled = false;
   int B = 0;
   int npad = 0;                // stacked rows padded to the MMA N granule
+  int sms = 0;                 // streaming multiprocessors of the device
   int splits[5] = {1, 1, 1, 1, 1};
   bool dense = true;
   int mpad = 0;                // rows allocated in the activation buffers
