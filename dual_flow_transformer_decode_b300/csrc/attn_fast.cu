@@ -326,10 +326,13 @@ __global__ void __launch_bounds__(160, 2)
   __syncthreads();
   ptx::grid_dep_launch();
 
-  // ---- merge the four warps (reuse the ring): mw[4][16], lw[4][16], ow[4][16][128]
+  // ---- merge the four warps (reuse the ring): mw, lw, ew [4][16] and the
+  // valid rows of ow [4][16][OWS] (row stride padded against bank conflicts)
+  constexpr int OWS = HD + 8;
   float* mw = reinterpret_cast<float*>(ring);
   float* lw = mw + 4 * RQ;
-  float* ow = lw + 4 * RQ;
+  float* ew = lw + 4 * RQ;
+  float* ow = ew + 4 * RQ;
   if (warp < 4) {
     if (tq == 0) {
       mw[warp * RQ + gq] = m_run[0];
@@ -340,64 +343,87 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int dcol = j * 8 + 2 * tq;
-      *reinterpret_cast<float2*>(ow + ((size_t)warp * RQ + gq) * HD + dcol) = make_float2(o[j][0], o[j][1]);
-      *reinterpret_cast<float2*>(ow + ((size_t)warp * RQ + gq + 8) * HD + dcol) = make_float2(o[j][2], o[j][3]);
+      if (gq < R)
+        *reinterpret_cast<float2*>(ow + ((size_t)warp * RQ + gq) * OWS + dcol) = make_float2(o[j][0], o[j][1]);
+      if (gq + 8 < R)
+        *reinterpret_cast<float2*>(ow + ((size_t)warp * RQ + gq + 8) * OWS + dcol) = make_float2(o[j][2], o[j][3]);
     }
   }
   __syncthreads();
   const bool aborted = *abort_flag != 0;
-  // CTA partial in cpart: M[16], L[16], O[16][128] (unnormalised)
-  for (int idx = tid; idx < R * HD; idx += blockDim.x) {
-    const int r = idx / HD, i = idx % HD;
+  // per row: the CTA maximum, each warp's weight relative to it, the sum
+  if (tid < R) {
+    const int r = tid;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * RQ + r]);
-    float acc = 0.f, l = 0.f;
+    float l = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const float mv = mw[w * RQ + r];
       const float e = (mv == -INFINITY) ? 0.f : expf(mv - M);
-      acc = fmaf(e, ow[((size_t)w * RQ + r) * HD + i], acc);
+      ew[w * RQ + r] = e;
       l = fmaf(e, lw[w * RQ + r], l);
     }
+    cpart[r] = M;
+    cpart[RQ + r] = l;
+  }
+  __syncthreads();
+  // CTA partial in cpart: M[16], L[16], O[16][128] (unnormalised)
+  for (int idx = tid; idx < R * HD; idx += blockDim.x) {
+    const int r = idx / HD, i = idx % HD;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc = fmaf(ew[w * RQ + r], ow[((size_t)w * RQ + r) * OWS + i], acc);
     cpart[2 * RQ + r * HD + i] = acc;
-    if (i == 0) {
-      cpart[r] = M;
-      cpart[RQ + r] = l;
-    }
   }
   // ---- merge the splits of the cluster, in split order; rank s writes the
-  // output elements [s*R*HD/splits, (s+1)*R*HD/splits)
+  // output elements [s*R*HD/splits, (s+1)*R*HD/splits).  Per row the splits'
+  // weights and the denominator are formed once (sew, sden), then each
+  // element reads only the splits' partial outputs.
   cl.sync();
+  float* sew = reinterpret_cast<float*>(ring);  // [kMaxSplits][16]
+  float* sden = sew + kMaxSplits * RQ;          // [16]
+  const int tot = R * HD, e0 = s * tot / splits, e1 = (s + 1) * tot / splits;
+  const int r0 = e0 / HD, r1 = e1 > e0 ? (e1 - 1) / HD + 1 : r0;
+  if (!aborted && tid < r1 - r0) {
+    const int r = r0 + tid;
+    float ms[kMaxSplits], ls[kMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < splits) {
+        const float* rp = cl.map_shared_rank(cpart, sp);
+        ms[sp] = rp[r];
+        ls[sp] = rp[RQ + r];
+      }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < splits) M = fmaxf(M, ms[sp]);
+    float den = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+      if (sp < splits) {
+        const float e = ms[sp] != -INFINITY ? expf(ms[sp] - M) : 0.f;
+        sew[sp * RQ + r] = e;
+        den = fmaf(e, ls[sp], den);
+      }
+    sden[r] = den;
+  }
+  __syncthreads();
   if (!aborted) {
-    const int tot = R * HD, e0 = s * tot / splits, e1 = (s + 1) * tot / splits;
     for (int idx = e0 + tid; idx < e1; idx += blockDim.x) {
       const int r = idx / HD, i = idx % HD;
-      float ms[kMaxSplits], ls[kMaxSplits], os[kMaxSplits];
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplits; ++sp) {
-        if (sp < splits) {
-          const float* rp = cl.map_shared_rank(cpart, sp);
-          ms[sp] = rp[r];
-          ls[sp] = rp[RQ + r];
-          os[sp] = rp[2 * RQ + r * HD + i];
-        }
-      }
-      float M = -INFINITY;
+      float os[kMaxSplits];
 #pragma unroll
       for (int sp = 0; sp < kMaxSplits; ++sp)
-        if (sp < splits) M = fmaxf(M, ms[sp]);
-      float den = 0.f, acc = 0.f;
+        if (sp < splits) os[sp] = cl.map_shared_rank(cpart, sp)[2 * RQ + r * HD + i];
+      float acc = 0.f;
 #pragma unroll
-      for (int sp = 0; sp < kMaxSplits; ++sp) {
-        if (sp < splits && ms[sp] != -INFINITY) {
-          const float e = expf(ms[sp] - M);
-          den = fmaf(e, ls[sp], den);
-          acc = fmaf(e, os[sp], acc);
-        }
-      }
+      for (int sp = 0; sp < kMaxSplits; ++sp)
+        if (sp < splits) acc = fmaf(sew[sp * RQ + r], os[sp], acc);
       const int f = flo + r / G, j = r % G;
-      out[(size_t)(f * B + b) * qdim + (g * G + j) * HD + i] = __float2bfloat16_rn(acc / den);
+      out[(size_t)(f * B + b) * qdim + (g * G + j) * HD + i] = __float2bfloat16_rn(acc / sden[r]);
     }
   }
   // keep this CTA's partial alive until the whole cluster has read it
@@ -406,7 +432,7 @@ __global__ void __launch_bounds__(160, 2)
 
 size_t smem_bytes(int NS) {
   size_t ring = (size_t)NS * STAGE;
-  size_t merge = (size_t)(2 * 4 * RQ + 4 * RQ * HD) * 4;  // reuses the ring after the loop
+  size_t merge = (size_t)(3 * 4 * RQ + 4 * RQ * (HD + 8)) * 4;  // reuses the ring after the loop
   if (merge > ring) ring = merge;
   return 1024 + ring + (size_t)RQ * HD * 2 + (size_t)(2 * RQ + RQ * HD) * 4 + 2 * NSMAX * 8 + 16;
 }
