@@ -255,8 +255,11 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
 }
 
 // One CTA = one K-split of one 128-row weight tile; the K-splits of a tile
-// form a thread-block cluster (cluster rank = split index).
-__global__ void __launch_bounds__(128, 1)
+// form a thread-block cluster (cluster rank = split index).  NT threads:
+// warp 0 TMA producer, warp 1 MMA issuer, all of them drain TMEM and run the
+// epilogue (256 when the footprint allows one CTA per SM anyway: wide N).
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, int N, int kblocks,
               int kStages, EpArgs ep, Ctrl* ctrl) {
   extern __shared__ uint8_t smem_raw[];
@@ -368,11 +371,13 @@ __global__ void __launch_bounds__(128, 1)
   const bool aborted = flags[0] != 0;
 
   if (!aborted) {
-    // TMEM -> partial tile st[column j][weight row r]
-    const int r = warp * 32 + lane;
-    for (int j0 = 0; j0 < N; j0 += 16) {
+    // TMEM -> partial tile st[column j][weight row r]; warp w reads TMEM
+    // lanes 32 (w % 4) .. +31, warps sharing a lane quarter split the
+    // 16-column chunks
+    const int quarter = warp & 3, r = quarter * 32 + lane;
+    for (int j0 = (warp >> 2) * 16; j0 < N; j0 += 16 * (NT / 128)) {
       float v[16];
-      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + j0, v);
+      ptx::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + j0, v);
 #pragma unroll
       for (int q = 0; q < 16; ++q) st[(j0 + q) * kBM + r] = v[q];
     }
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(128, 1)
   // Every CTA of the cluster has its partial tile in shared memory after this.
   cl.sync();
   ptx::grid_dep_launch();
-  if (!aborted) epilogue(ep, cl, st, par, S, tile * kBM, p0, p1, tid, 128);
+  if (!aborted) epilogue(ep, cl, st, par, S, tile * kBM, p0, p1, tid, NT);
   // Keep this CTA's shared memory alive until the whole cluster has read it.
   cl.sync();
   if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
@@ -494,8 +499,10 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   P.o_ptr = Bf.o;
   P.z_ptr = Bf.z;
   P.mpad = Mpad;
-  cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(k_tc_gemm<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaFuncSetAttribute(k_tc_gemm<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(k_tc_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaFuncSetAttribute(k_tc_gemm<256>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   P.enabled = true;
   P.dense = !D.E;
   return true;
@@ -580,7 +587,14 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n
   at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   lc.attrs = at;
   lc.numAttrs = 2;
-  cudaLaunchKernelEx(&lc, k_tc_gemm, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
+  // a footprint above half the SM already means one CTA per SM: use the
+  // wider CTA, whose extra warps share the epilogue
+  if (lc.dynamicSmemBytes > 114 * 1024) {
+    lc.blockDim = dim3(256);
+    cudaLaunchKernelEx(&lc, k_tc_gemm<256>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
+  } else {
+    cudaLaunchKernelEx(&lc, k_tc_gemm<128>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
+  }
 }
 
 }  // namespace
