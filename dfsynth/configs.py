@@ -44,6 +44,7 @@ class DFConfig:
     gain_std: float = 0.0    # norm gains are 1 + N(0, gain_std)
     router_std: float = -1.0  # <0 means 1/sqrt(d_model)
     lm_scale: float = 1.0    # multiplies the LM-head draw (peaked-logit tests)
+    aux_top_k: int = 0       # MoE auxiliary fan-out (0: the auxiliary flow replays the primary's top_k)
 
     @property
     def max_len(self) -> int:
@@ -68,6 +69,12 @@ class DFConfig:
     @property
     def mlp_hidden(self) -> int:
         return self.expert_hidden if self.is_moe else self.ffn_hidden
+
+    @property
+    def aux_k(self) -> int:
+        """Experts the auxiliary flow uses per token: the primary's top_k
+        (replayed) plus aux_top_k - top_k chosen from its own router logits."""
+        return max(self.aux_top_k, self.top_k) if self.is_moe else 0
 
     @property
     def router_sigma(self) -> float:
@@ -128,6 +135,18 @@ TEST_CONFIGS = {
                       head_dim=128, ffn_hidden=0, vocab=1000, dtype="bf16",
                       batch=5, n_prefill=33, n_steps=5, n_experts=8, top_k=2,
                       expert_hidden=192, gain_std=0.1),
+    # independent auxiliary fan-out: 2 replayed + 2 own experts per token
+    "t_moe_fan": DFConfig("t_moe_fan", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
+                          head_dim=128, ffn_hidden=0, vocab=1000, dtype="bf16",
+                          batch=5, n_prefill=33, n_steps=5, n_experts=8, top_k=2,
+                          expert_hidden=192, gain_std=0.1, aux_top_k=4),
+}
+
+# Workload variants measured beside the named workloads (not parity cases).
+VARIANTS = {
+    # the MoE workload with the auxiliary flow using 8 experts per token
+    # (4 replayed + 4 of its own): decode compute grows, prefill does not
+    "moe64e_top4_aux8": WORKLOADS["moe64e_top4"].with_(name="moe64e_top4_aux8", aux_top_k=8),
 }
 
 
@@ -136,4 +155,6 @@ def get_config(name: str) -> DFConfig:
         return WORKLOADS[name]
     if name in TEST_CONFIGS:
         return TEST_CONFIGS[name]
-    raise KeyError(f"unknown config {name!r}; known: {sorted(WORKLOADS) + sorted(TEST_CONFIGS)}")
+    if name in VARIANTS:
+        return VARIANTS[name]
+    raise KeyError(f"unknown config {name!r}; known: {sorted(WORKLOADS) + sorted(TEST_CONFIGS) + sorted(VARIANTS)}")

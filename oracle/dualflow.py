@@ -25,7 +25,15 @@ step below that the pages leave open follows one stated reading:
   residual unrounded; the primary takes the top-k logits (descending, ties to
   the lower index); each flow's gates are the softmax of its own router
   logits over that set; one b of the expert hidden size is shared by all
-  experts of a layer; no capacity limit.
+  experts of a layer; no capacity limit;
+* independent auxiliary fan-out ("Contribuciones Clave" 3 and "Significado y
+  Reivindicaciones": each flow's expert fan-out is configurable): with
+  aux_top_k = k_a > k the auxiliary flow keeps the replayed set S and adds
+  the k_a - k largest of its own router logits among the experts outside S
+  (ties to the lower index); its gates are the softmax of its router logits
+  over S followed by those extra experts; the b coupling applies to the
+  replayed experts only (the primary computed no hidden state for the
+  others).
 
 Quantisation points (mirrored by the GPU): in bf16 models the GEMM inputs,
 the KV-cache stores and the attention queries are rounded to bf16
@@ -213,6 +221,23 @@ class Oracle:
     def _expert_hidden(self, l, e, u):
         return silu(u @ self.EW(l, e, "wg").T) * (u @ self.EW(l, e, "wu").T)
 
+    @staticmethod
+    def _aux_extra(r2: np.ndarray, S: np.ndarray, nx: int) -> np.ndarray:
+        """The auxiliary flow's own nx experts: its largest router logits among
+        the experts outside the replayed set S (descending, ties to the lower
+        index)."""
+        if nx <= 0:
+            return np.zeros(0, dtype=np.int64)
+        rest = [e for e in range(len(r2)) if e not in set(int(x) for x in S)]
+        order = sorted(rest, key=lambda e: (-float(r2[e]), e))
+        return np.array(order[:nx], dtype=np.int64)
+
+    @staticmethod
+    def _aux_extra_margin(r2: np.ndarray, S: np.ndarray, nx: int) -> float:
+        """Gap between the last chosen and the first unchosen of those logits."""
+        rest = sorted((float(r2[e]) for e in range(len(r2)) if e not in set(int(x) for x in S)), reverse=True)
+        return rest[nx - 1] - rest[nx] if len(rest) > nx else np.inf
+
     def _router(self, l, h):
         cfg = self.cfg
         return rmsnorm(h, self.W(l, "mlp_norm"), cfg.norm_eps) @ self.W(l, "router").T
@@ -303,6 +328,7 @@ class Oracle:
         topk_sets = np.zeros((L, self.nb, max(cfg.top_k, 1)), dtype=np.int64)
         topk_margin = np.full((L, self.nb), np.inf)
         router_logits = []
+        ptrace = []
         for l in range(L):
             u = self.q(rmsnorm(h1, self.W(l, "attn_norm"), cfg.norm_eps))
             q1 = u @ self.W(l, "wq").T                          # pre-RoPE, fp64
@@ -315,6 +341,8 @@ class Oracle:
                 qr = self.qa(rope(self._heads(q1[s], cfg.n_heads), t, cfg.rope_theta))
                 o1[s] = attend(qr, self.K[l][s][:, :t + 1], self.V[l][s][:, :t + 1]).reshape(-1)
             h1 = h1 + self.q(o1) @ self.W(l, "wo").T
+            if trace:
+                ptrace.append({"h1_attn": h1.copy()})
             if cfg.is_moe:
                 r1 = self._router(l, h1)
                 u2 = self.q(rmsnorm(h1, self.W(l, "mlp_norm"), cfg.norm_eps))
@@ -354,6 +382,9 @@ class Oracle:
         if aux:
             # ---- auxiliary flow: reads the primary cache and saved state ----
             h2 = self.W("emb2")[tok].copy()
+            nxa = max(cfg.aux_k - cfg.top_k, 0) if cfg.is_moe else 0
+            aux_extra = np.zeros((L, self.nb, nxa), dtype=np.int64)
+            aux_margin = np.full((L, self.nb), np.inf)
             tr = []
             for l in range(L):
                 sv = saved[l]
@@ -369,11 +400,19 @@ class Oracle:
                     r2 = self._router(l, h2)
                     u2 = self.q(rmsnorm(h2, self.W(l, "mlp_norm"), cfg.norm_eps))
                     y2 = np.zeros_like(h2)
+                    nx = cfg.aux_k - cfg.top_k
                     for s in range(self.nb):
                         S = sv["sets"][s]
-                        g2 = np.exp(log_softmax(r2[s][S]))
-                        for j, e in enumerate(S):
-                            z = self._expert_hidden(l, e, u2[s:s + 1])[0] + self.W(l, "b") * sv["z1"][(s, j)]
+                        X = self._aux_extra(r2[s], S, nx)
+                        aux_extra[l, s] = X
+                        if nx > 0:
+                            aux_margin[l, s] = self._aux_extra_margin(r2[s], S, nx)
+                        SA = np.concatenate([S, X]).astype(np.int64)
+                        g2 = np.exp(log_softmax(r2[s][SA]))
+                        for j, e in enumerate(SA):
+                            z = self._expert_hidden(l, e, u2[s:s + 1])[0]
+                            if j < len(S):
+                                z = z + self.W(l, "b") * sv["z1"][(s, j)]
                             y2[s] += g2[j] * (self.q(z) @ self.EW(l, e, "wd").T)
                     y2 = y2 + self.W(l, "c") * sv["y1"]
                 else:
@@ -391,6 +430,9 @@ class Oracle:
                 mix[s], alpha[s] = mixture(logp1[s], logp2[s])
             out["logits2"] = logits2
             out["logp2"] = logp2
+            if cfg.is_moe:
+                out["topk_aux"] = aux_extra
+                out["topk_aux_margin"] = aux_margin
             out["logp_mix"] = mix
             out["alpha"] = alpha
             out["argmax"] = np.argmax(mix, axis=1)
@@ -398,6 +440,7 @@ class Oracle:
             out["argmax_margin"] = srt[:, -1] - srt[:, -2]
             if trace:
                 out["trace"] = tr
+                out["trace_primary"] = ptrace
         srt1 = np.sort(logp1, axis=1)
         out["argmax1_margin"] = srt1[:, -1] - srt1[:, -2]
         self.t = t + 1

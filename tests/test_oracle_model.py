@@ -218,3 +218,103 @@ def test_primary_flow_is_a_standard_transformer(name):
         for l in range(cfg.n_layers):
             np.testing.assert_allclose(o.K[l][s][:, :P], Ks[l], rtol=0, atol=1e-12)
             np.testing.assert_allclose(o.V[l][s][:, :P], Vs[l], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- auxiliary fan-out
+
+def _aux_moe_layer0_by_hand(cfg, w, tr_primary, tr_aux, nx_pick):
+    """Layer 0's auxiliary MoE written out independently of the oracle's
+    routing code: the primary set by sorting, the auxiliary extras by
+    `nx_pick(r2, S)`, softmax over the union, b coupling only on the
+    replayed experts, c coupling of the primary output.  Returns h2 after
+    the layer."""
+    bf = lambda x: x  # noqa: E731 — fp32 parity config: no rounding points
+    if cfg.dtype == "bf16":
+        from oracle import bf16_rne as bf
+    d = cfg.d_model
+
+    def rms(x, g):
+        return x / np.sqrt(np.mean(x * x) + cfg.norm_eps) * g
+
+    def hidden(e, u):
+        wg = np.asarray(w[(0, e, "wg")], np.float64)
+        wu = np.asarray(w[(0, e, "wu")], np.float64)
+        a, b = wg @ u, wu @ u
+        return a / (1 + np.exp(-a)) * b
+
+    g_mlp = np.asarray(w[(0, "mlp_norm")], np.float64)
+    Wr = np.asarray(w[(0, "router")], np.float64)
+    bvec = np.asarray(w[(0, "b")], np.float64)
+    cvec = np.asarray(w[(0, "c")], np.float64)
+    out = []
+    for s in range(tr_aux[0]["h2_attn"].shape[0]):
+        h1 = tr_primary[0]["h1_attn"][s]
+        h2 = tr_aux[0]["h2_attn"][s]
+        r1 = Wr @ rms(h1, g_mlp)
+        S = sorted(range(cfg.n_experts), key=lambda e: (-r1[e], e))[:cfg.top_k]
+        u1 = bf(rms(h1, g_mlp))
+        p1 = np.exp(r1[S] - r1[S].max())
+        p1 /= p1.sum()
+        z1 = {e: hidden(e, u1) for e in S}
+        y1 = sum(p1[j] * (np.asarray(w[(0, e, "wd")], np.float64) @ bf(z1[e])) for j, e in enumerate(S))
+        r2 = Wr @ rms(h2, g_mlp)
+        SA = list(S) + list(nx_pick(r2, S))
+        p2 = np.exp(r2[SA] - r2[SA].max())
+        p2 /= p2.sum()
+        u2 = bf(rms(h2, g_mlp))
+        y2 = np.zeros(d)
+        for j, e in enumerate(SA):
+            z = hidden(e, u2) + (bvec * z1[e] if e in S else 0.0)
+            y2 += p2[j] * (np.asarray(w[(0, e, "wd")], np.float64) @ bf(z))
+        out.append(h2 + y2 + cvec * y1)
+    return np.stack(out)
+
+
+@pytest.mark.parametrize("aux_top_k", [4, 8])
+def test_aux_fanout_layer_written_out(aux_top_k):
+    """Independent fan-out: the oracle's auxiliary MoE layer against the same
+    layer written out by hand — the extras are the largest auxiliary router
+    logits outside the replayed set (aux_top_k = E: every expert, a dense
+    softmax mixture), gates are a softmax over the union, and only replayed
+    experts carry the b coupling."""
+    cfg = dfsynth.get_config("t_moe").with_(n_layers=1, n_steps=1, aux_top_k=aux_top_k, dtype="f32")
+    w = Weights(cfg, 0)
+    _, outs = _run(cfg, w, trace=True)
+    r = outs[0]
+    nx = aux_top_k - cfg.top_k
+
+    def pick(r2, S):
+        rest = [e for e in range(cfg.n_experts) if e not in S]
+        return sorted(rest, key=lambda e: (-r2[e], e))[:nx]
+
+    ref = _aux_moe_layer0_by_hand(cfg, w, r["trace_primary"], r["trace"], pick)
+    np.testing.assert_allclose(r["trace"][0]["h2"], ref, rtol=1e-10, atol=1e-12)
+    assert r["topk_aux"].shape == (1, cfg.batch, nx)
+    for s in range(cfg.batch):
+        assert not set(r["topk_aux"][0, s]) & set(r["topk"][0, s])
+
+
+def test_aux_fanout_equal_to_top_k_is_replay():
+    """aux_top_k = top_k: exactly the router-replay model."""
+    cfg = dfsynth.get_config("t_moe").with_(n_steps=2)
+    w = Weights(cfg, 0)
+    _, a = _run(cfg, w)
+    _, b = _run(cfg.with_(aux_top_k=cfg.top_k), w)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x["logp_mix"], y["logp_mix"])
+
+
+def test_aux_fanout_leaves_primary_unchanged():
+    """The auxiliary flow's extra experts change nothing the primary computes
+    (cache, primary log-probabilities, primary sets)."""
+    cfg = dfsynth.get_config("t_moe_fan").with_(n_steps=2)
+    w = Weights(cfg, 0)
+    oa, a = _run(cfg, w)
+    ob, b = _run(cfg.with_(aux_top_k=0), w)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x["logp1"], y["logp1"])
+        np.testing.assert_array_equal(x["topk"], y["topk"])
+        assert not np.array_equal(x["logp2"], y["logp2"])
+    for l in range(cfg.n_layers):
+        for s in range(cfg.batch):
+            np.testing.assert_array_equal(oa.K[l][s], ob.K[l][s])
