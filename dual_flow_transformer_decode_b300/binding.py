@@ -23,7 +23,7 @@ class df_config(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim",
                                        "ffn_hidden", "vocab", "n_experts", "top_k", "expert_hidden")] + [
         ("rope_theta", C.c_float), ("norm_eps", C.c_float), ("dtype", C.c_int),
-        ("max_batch", C.c_int), ("max_len", C.c_int)]
+        ("max_batch", C.c_int), ("max_len", C.c_int), ("aux_top_k", C.c_int)]
 
 
 class df_weights(C.Structure):
@@ -102,7 +102,8 @@ def make_config(cfg, max_batch: int, max_len: int) -> df_config:
     return df_config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
                      cfg.ffn_hidden if not cfg.n_experts else 0, cfg.vocab, cfg.n_experts, cfg.top_k,
                      cfg.expert_hidden, float(cfg.rope_theta), float(cfg.norm_eps),
-                     DF_BF16 if cfg.dtype == "bf16" else DF_F32, max_batch, max_len)
+                     DF_BF16 if cfg.dtype == "bf16" else DF_F32, max_batch, max_len,
+                     getattr(cfg, "aux_top_k", 0) if cfg.n_experts else 0)
 
 
 def df_workspace_bytes(c: df_config) -> tuple[int, int]:

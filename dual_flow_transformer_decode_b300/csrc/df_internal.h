@@ -35,6 +35,7 @@ inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Model dimensions plus derived sizes, fixed at df_create.
 struct Dims {
   int L, d, Hq, Hkv, hd, F, V, E, k, Fe;
+  int ka;          // MoE experts per auxiliary token (>= k; k + auxiliary fan-out)
   float theta, eps;
   int bf16;        // 1: bf16 storage, 0: fp32
   int maxB, max_len;
@@ -64,12 +65,13 @@ struct Buffers {
   float* y1s;       // [L][maxB][d] saved primary MLP output
   float* rlog;      // [2maxB][E] router logits
   int* topk;        // [L][maxB][k] primary expert sets
-  float* gate;      // [2maxB][k] gate weights per row
+  float* gate;      // [2maxB][ka] gate weights per row (primary rows use the first k)
+  int* topkx;       // [maxB][ka-k] this layer's auxiliary-own experts
   int* ecount;      // [E]
-  int* elist;       // [E][maxB] entries b*k + j
-  void* zE;         // [2][maxB][k][Fe] expert hidden (dtype)
-  float* yE;        // [2][maxB][k][d] expert outputs fp32
-  int* eslot;       // [maxB][k] position of entry b*k+j in its expert's list
+  int* elist;       // [E][maxB] entries: b*k + j (replayed), B*k + b*(ka-k) + j (auxiliary-own)
+  void* zE;         // [2][maxB][ka][Fe] expert hidden (dtype)
+  float* yE;        // [2][maxB][ka][d] expert outputs fp32
+  int* eslot;       // [maxB*ka] position of each entry in its expert's list
   void* xg;         // [E][nxe][d] packed expert input rows (tensor-core MoE path)
   void* zEt;        // [E][nxe][Fe] packed expert hidden rows
   float* yEt;       // [E][nxe][d] packed expert outputs

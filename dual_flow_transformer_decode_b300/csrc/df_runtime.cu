@@ -124,6 +124,8 @@ bool valid_config(const df_config* c, std::string* why) {
   } else {
     if (c->top_k <= 0 || c->top_k > c->n_experts || c->top_k > 16) return bad("top_k must be in [1, min(16, E)]");
     if (c->expert_hidden <= 0 || c->expert_hidden % 64) return bad("expert_hidden must be a positive multiple of 64");
+    if (c->aux_top_k && (c->aux_top_k < c->top_k || c->aux_top_k > c->n_experts || c->aux_top_k > 16))
+      return bad("aux_top_k must be 0 or in [top_k, min(16, E)]");
   }
   if (c->n_experts > 4096) return bad("n_experts above 4096");
   if (!(c->norm_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("norm_eps and rope_theta must be positive");
@@ -141,6 +143,7 @@ Dims make_dims(const df_config* c) {
   D.V = c->vocab;
   D.E = c->n_experts;
   D.k = c->n_experts ? c->top_k : 0;
+  D.ka = c->n_experts ? (c->aux_top_k > c->top_k ? c->aux_top_k : c->top_k) : 0;
   D.Fe = c->n_experts ? c->expert_hidden : 0;
   D.theta = c->rope_theta;
   D.eps = c->norm_eps;
@@ -201,12 +204,13 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.y1s = (float*)take((size_t)D.L * D.maxB * D.d * 4);
   b.rlog = (float*)take(D.E ? M2 * D.E * 4 : 0);
   b.topk = (int*)take(D.E ? (size_t)D.L * D.maxB * D.k * 4 : 0);
-  b.gate = (float*)take(D.E ? M2 * D.k * 4 : 0);
+  b.gate = (float*)take(D.E ? M2 * D.ka * 4 : 0);
+  b.topkx = (int*)take(D.E ? (size_t)D.maxB * (D.ka - D.k) * 4 : 0);
   b.ecount = (int*)take(D.E * 4);
   b.elist = (int*)take((size_t)D.E * D.maxB * 4);
-  b.zE = take(D.E ? 2 * (size_t)D.maxB * D.k * D.Fe * esz : 0);
-  b.yE = (float*)take(D.E ? 2 * (size_t)D.maxB * D.k * D.d * 4 : 0);
-  b.eslot = (int*)take(D.E ? (size_t)D.maxB * D.k * 4 : 0);
+  b.zE = take(D.E ? 2 * (size_t)D.maxB * D.ka * D.Fe * esz : 0);
+  b.yE = (float*)take(D.E ? 2 * (size_t)D.maxB * D.ka * D.d * 4 : 0);
+  b.eslot = (int*)take(D.E ? (size_t)D.maxB * D.ka * 4 : 0);
   const size_t nxe = D.E ? (size_t)df::moe_nxe(D) : 0;
   b.xg = take(D.E * nxe * D.d * esz);
   b.zEt = take(D.E * nxe * D.Fe * esz);

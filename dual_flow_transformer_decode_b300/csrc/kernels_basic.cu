@@ -797,82 +797,123 @@ void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows&
 
 // The primary rows choose their top-k experts (descending router logit,
 // ties to the lower index); each flow's gates are the softmax of its own
-// router logits over that set ("Mecanismos Clave", Replay de Router).  The
-// per-expert entry lists (b*k + j, ascending b) let every selected expert's
-// weights be read once for both flows.
+// router logits over that set ("Mecanismos Clave", Replay de Router).  With
+// an independent auxiliary fan-out (ka > k; "Contribuciones Clave" 3) the
+// auxiliary row also takes its own ka - k largest router logits among the
+// other experts, and its gates are the softmax over the replayed set
+// followed by those.  Entries: b*k + j (replayed; both flows' rows) and
+// B*k + b*(ka-k) + j (auxiliary-own; the auxiliary row only).  The
+// per-expert entry lists (ascending entry) let every selected expert's
+// weights be read once for all rows that use it; an expert is either
+// replayed or auxiliary-own for a sequence, never both, so a list holds at
+// most B entries.
 
-__global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, float* __restrict__ gate,
-                            int* __restrict__ ecount, int* __restrict__ elist, int* __restrict__ eslot, int B, int E,
-                            int k, int maxB, int select, int prim, int aux, int32_t* __restrict__ dbg_topk_l,
-                            float* __restrict__ dbg_router_l) {
+// Warp-wide argmax over experts e = lane, lane+32, ... not in the taken
+// bitmasks (larger value wins, equal values -> lower index).
+__device__ __forceinline__ int warp_pick(const float* r, int E, int lane, unsigned long long tlo,
+                                         unsigned long long thi) {
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  int q = 0;
+  for (int e = lane; e < E; e += 32, ++q) {
+    const bool tk = q < 64 ? ((tlo >> q) & 1ull) : ((thi >> (q - 64)) & 1ull);
+    if (tk) continue;
+    const float v = r[e];
+    if (v > best || (v == best && e < bi)) {
+      best = v;
+      bi = e;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  return bi;
+}
+
+__device__ __forceinline__ void mark_taken(int e, int lane, unsigned long long& tlo, unsigned long long& thi) {
+  if (e != 0x7fffffff && (e % 32) == lane) {
+    const int qq = e / 32;
+    if (qq < 64)
+      tlo |= 1ull << qq;
+    else
+      thi |= 1ull << (qq - 64);
+  }
+}
+
+// Softmax gates of `n` entries held by lanes 0..n-1 (max and sum in entry order).
+__device__ __forceinline__ float entry_gate(float v, int n, int lane) {
+  float mx = -INFINITY;
+  for (int j = 0; j < n; ++j) mx = fmaxf(mx, __shfl_sync(0xffffffffu, v, j));
+  const float ex = lane < n ? expf(v - mx) : 0.f;
+  float den = 0.f;
+  for (int j = 0; j < n; ++j) den += __shfl_sync(0xffffffffu, ex, j);
+  return ex / den;
+}
+
+__global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, int* __restrict__ topkx,
+                            float* __restrict__ gate, int* __restrict__ ecount, int* __restrict__ elist,
+                            int* __restrict__ eslot, int B, int E, int k, int ka, int maxB, int select, int prim,
+                            int aux, int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // one warp per primary row: k rounds of a warp-wide argmax (larger value
-  // wins, equal values -> lower index) over the experts not yet taken
+  const int kx = aux ? ka - k : 0;  // auxiliary-own experts per token
+  // one warp per sequence
   for (int b = w; b < B; b += warps) {
-    int sel = 0;  // lane j < k: the j-th selected expert
+    int sel = 0;  // lane j < k: the j-th replayed expert
+    unsigned long long tlo = 0ull, thi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
     if (select) {
       const float* r = rlog + (size_t)b * E;
-      unsigned long long taken_lo = 0ull, taken_hi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
       for (int j = 0; j < k; ++j) {
-        float best = -INFINITY;
-        int bi = 0x7fffffff;
-        int q = 0;
-        for (int e = lane; e < E; e += 32, ++q) {
-          const bool tk = q < 64 ? ((taken_lo >> q) & 1ull) : ((taken_hi >> (q - 64)) & 1ull);
-          if (tk) continue;
-          const float v = r[e];
-          if (v > best || (v == best && e < bi)) {
-            best = v;
-            bi = e;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > best || (ov == best && oi < bi)) {
-            best = ov;
-            bi = oi;
-          }
-        }
+        const int bi = warp_pick(r, E, lane, tlo, thi);
         if (lane == 0) topk_l[b * k + j] = bi;
         if (lane == j) sel = bi;
-        if (bi != 0x7fffffff && (bi % 32) == lane) {
-          const int qq = bi / 32;
-          if (qq < 64)
-            taken_lo |= 1ull << qq;
-          else
-            taken_hi |= 1ull << (qq - 64);
-        }
+        mark_taken(bi, lane, tlo, thi);
       }
-    } else if (lane < k) {
-      sel = topk_l[b * k + lane];
+    } else {
+      if (lane < k) sel = topk_l[b * k + lane];
+      for (int j = 0; j < k; ++j) mark_taken(__shfl_sync(0xffffffffu, sel, j), lane, tlo, thi);
     }
-    // gates: lane j holds entry j; max and sum taken in entry order
-    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
-      const float* r = rlog + (size_t)(f * B + b) * E;
-      const float v = lane < k ? r[sel] : -INFINITY;
-      float mx = -INFINITY;
-      for (int j = 0; j < k; ++j) mx = fmaxf(mx, __shfl_sync(0xffffffffu, v, j));
-      const float ex = lane < k ? expf(v - mx) : 0.f;
-      float den = 0.f;
-      for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ex, j);
-      if (lane < k) gate[(size_t)(f * B + b) * k + lane] = ex / den;
+    // primary gates over the replayed set
+    if (prim) {
+      const float* r = rlog + (size_t)b * E;
+      const float g = entry_gate(lane < k ? r[sel] : -INFINITY, k, lane);
+      if (lane < k) gate[(size_t)b * ka + lane] = g;
     }
-    if (dbg_topk_l && prim && lane < k) dbg_topk_l[b * k + lane] = sel;
+    // auxiliary: its own experts outside the replayed set, gates over the union
+    int own = 0;  // lane k + j: the j-th auxiliary-own expert
+    if (aux) {
+      const float* r = rlog + (size_t)(B + b) * E;
+      for (int j = 0; j < kx; ++j) {
+        const int bi = warp_pick(r, E, lane, tlo, thi);
+        if (lane == 0) topkx[b * kx + j] = bi;
+        if (lane == k + j) own = bi;
+        mark_taken(bi, lane, tlo, thi);
+      }
+      const int ent = lane < k ? sel : own;
+      const float g = entry_gate(lane < k + kx ? r[ent] : -INFINITY, k + kx, lane);
+      if (lane < k + kx) gate[(size_t)(B + b) * ka + lane] = g;
+      if (dbg_topk_l && lane >= k && lane < k + kx) dbg_topk_l[b * ka + lane] = own;
+    }
+    if (dbg_topk_l && prim && lane < k) dbg_topk_l[b * ka + lane] = sel;
     if (dbg_router_l && prim)
       for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
   }
   __syncthreads();
   // entry lists in ascending entry order: warp per expert, 32 entries a round
-  const int nent = B * k;
+  const int nent = B * k + B * kx;
   for (int e = w; e < E; e += warps) {
     int cnt = 0;
     for (int base = 0; base < nent; base += 32) {
       const int idx = base + lane;
-      const bool hit = idx < nent && topk_l[idx] == e;
+      const int ex = idx < B * k ? topk_l[idx] : idx < nent ? topkx[idx - B * k] : -1;
+      const bool hit = idx < nent && ex == e;
       const unsigned m = __ballot_sync(0xffffffffu, hit);
       if (hit) {
         const int slot = cnt + __popc(m & ((1u << lane) - 1u));
@@ -888,11 +929,10 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
 void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
                       float* dbg_router, cudaStream_t s) {
   int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_route, dim3(1), dim3(1024), 0, s, Bf.rlog, topk_l, Bf.gate, Bf.ecount, Bf.elist, Bf.eslot, R.B, D.E,
-             D.k, D.maxB, select,
-                                R.has_primary(), R.has_aux(),
-                                dbg_topk ? dbg_topk + (size_t)layer * R.B * D.k : nullptr,
-                                dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);
+  launch_pdl(k_moe_route, dim3(1), dim3(1024), 0, s, Bf.rlog, topk_l, Bf.topkx, Bf.gate, Bf.ecount, Bf.elist,
+             Bf.eslot, R.B, D.E, D.k, D.ka, D.maxB, select, R.has_primary(), R.has_aux(),
+             dbg_topk ? dbg_topk + (size_t)layer * R.B * D.ka : nullptr,
+             dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);
 }
 
 // Expert gate/up + SwiGLU + b coupling (CUDA cores): one warp per expert
@@ -900,7 +940,7 @@ void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, c
 template <typename T>
 __global__ void k_moe_gateup(const T* __restrict__ wgu, const float* __restrict__ bvec, const T* __restrict__ u,
                              const int* __restrict__ ecount, const int* __restrict__ elist, T* __restrict__ zE,
-                             Couple C, int B, int d, int Fe, int k, int maxB, int prim, int aux) {
+                             Couple C, int B, int d, int Fe, int k, int ka, int maxB, int prim, int aux) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   int e = blockIdx.x;
@@ -913,10 +953,13 @@ __global__ void k_moe_gateup(const T* __restrict__ wgu, const float* __restrict_
   const T* wg = W + (size_t)((fi >> 6) * 128 + (fi & 63)) * d;
   const T* wu = wg + (size_t)64 * d;
   for (int idx = 0; idx < cnt; ++idx) {
-    int ent = elist[(size_t)e * maxB + idx];
-    int b = ent / k, j = ent % k;
+    const int ent = elist[(size_t)e * maxB + idx];
+    // replayed entry (both flows) or auxiliary-own entry (auxiliary row only)
+    const bool own = ent >= B * k;
+    const int b = own ? (ent - B * k) / (ka - k) : ent / k;
+    const int j = own ? k + (ent - B * k) % (ka - k) : ent % k;
     float z1 = 0.f;
-    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+    for (int f = (prim && !own) ? 0 : 1; f < (aux ? 2 : 1); ++f) {
       const T* x = u + (size_t)(f * B + b) * d;
       float ag = 0.f, au = 0.f;
       for (int kk = lane; kk < d; kk += 32) {
@@ -930,11 +973,11 @@ __global__ void k_moe_gateup(const T* __restrict__ wgu, const float* __restrict_
       if (f == 0) {
         z1 = zz;
         if (C.save && lane == 0) C.z1s[(size_t)ent * Fe + fi] = zz;
-      } else {
+      } else if (!own) {  // the b coupling exists for replayed experts only
         float p = C.saved ? C.z1s[(size_t)ent * Fe + fi] : z1;
         zz = fmaf(bvec[fi], p, zz);
       }
-      if (lane == 0) zE[((size_t)(f * maxB + b) * k + j) * Fe + fi] = Num<T>::from_f(zz);
+      if (lane == 0) zE[((size_t)(f * maxB + b) * ka + j) * Fe + fi] = Num<T>::from_f(zz);
     }
   }
 }
@@ -945,17 +988,17 @@ void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu
   if (D.bf16)
     launch_pdl(k_moe_gateup<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __nv_bfloat16*)wgu, bvec, (const __nv_bfloat16*)Bf.u,
                                                       Bf.ecount, Bf.elist, (__nv_bfloat16*)Bf.zE, C, R.B, D.d,
-                                                      D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
+                                                      D.Fe, D.k, D.ka, D.maxB, R.has_primary(), R.has_aux());
   else
     launch_pdl(k_moe_gateup<float>, dim3(grid), dim3(256), 0, s, (const float*)wgu, bvec, (const float*)Bf.u, Bf.ecount, Bf.elist,
-                                             (float*)Bf.zE, C, R.B, D.d, D.Fe, D.k, D.maxB, R.has_primary(),
+                                             (float*)Bf.zE, C, R.B, D.d, D.Fe, D.k, D.ka, D.maxB, R.has_primary(),
                                              R.has_aux());
 }
 
 template <typename T>
 __global__ void k_moe_down(const T* __restrict__ wd, const T* __restrict__ zE, const int* __restrict__ ecount,
-                           const int* __restrict__ elist, float* __restrict__ yE, int d, int Fe, int k, int maxB,
-                           int prim, int aux) {
+                           const int* __restrict__ elist, float* __restrict__ yE, int B, int d, int Fe, int k, int ka,
+                           int maxB, int prim, int aux) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   int e = blockIdx.x;
@@ -966,14 +1009,16 @@ __global__ void k_moe_down(const T* __restrict__ wd, const T* __restrict__ zE, c
   if (n >= d) return;
   const T* wr = wd + ((size_t)e * d + n) * Fe;
   for (int idx = 0; idx < cnt; ++idx) {
-    int ent = elist[(size_t)e * maxB + idx];
-    int b = ent / k, j = ent % k;
-    for (int f = prim ? 0 : 1; f < (aux ? 2 : 1); ++f) {
-      const T* z = zE + ((size_t)(f * maxB + b) * k + j) * Fe;
+    const int ent = elist[(size_t)e * maxB + idx];
+    const bool own = ent >= B * k;
+    const int b = own ? (ent - B * k) / (ka - k) : ent / k;
+    const int j = own ? k + (ent - B * k) % (ka - k) : ent % k;
+    for (int f = (prim && !own) ? 0 : 1; f < (aux ? 2 : 1); ++f) {
+      const T* z = zE + ((size_t)(f * maxB + b) * ka + j) * Fe;
       float acc = 0.f;
       for (int kk = lane; kk < Fe; kk += 32) acc = fmaf(Num<T>::to_f(wr[kk]), Num<T>::to_f(z[kk]), acc);
       acc = warp_sum(acc);
-      if (lane == 0) yE[((size_t)(f * maxB + b) * k + j) * d + n] = acc;
+      if (lane == 0) yE[((size_t)(f * maxB + b) * ka + j) * d + n] = acc;
     }
   }
 }
@@ -982,32 +1027,33 @@ void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, c
   dim3 grid(D.E, (D.d + 7) / 8);
   if (D.bf16)
     launch_pdl(k_moe_down<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __nv_bfloat16*)wd, (const __nv_bfloat16*)Bf.zE,
-                                                    Bf.ecount, Bf.elist, Bf.yE, D.d, D.Fe, D.k, D.maxB,
-                                                    R.has_primary(), R.has_aux());
+                                                    Bf.ecount, Bf.elist, Bf.yE, R.B, D.d, D.Fe, D.k, D.ka,
+                                                    D.maxB, R.has_primary(), R.has_aux());
   else
-    launch_pdl(k_moe_down<float>, dim3(grid), dim3(256), 0, s, (const float*)wd, (const float*)Bf.zE, Bf.ecount, Bf.elist, Bf.yE, D.d,
-                                           D.Fe, D.k, D.maxB, R.has_primary(), R.has_aux());
+    launch_pdl(k_moe_down<float>, dim3(grid), dim3(256), 0, s, (const float*)wd, (const float*)Bf.zE, Bf.ecount, Bf.elist, Bf.yE, R.B,
+                                           D.d, D.Fe, D.k, D.ka, D.maxB, R.has_primary(), R.has_aux());
 }
 
 // y_f = sum_j gate_f[j] * yE_f[j] (slot order), y2 += c ⊙ y1, h += y.
 __global__ void k_moe_combine(const float* __restrict__ yE, const float* __restrict__ gate,
                               const float* __restrict__ cvec, float* __restrict__ h, Couple C, int B, int lo, int d,
-                              int k, int maxB) {
+                              int k, int ka, int maxB) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
+  const int kr = f ? ka : k;  // entries of this row: the replayed ones, then the auxiliary-own ones
   for (int n = threadIdx.x; n < d; n += blockDim.x) {
     float y = 0.f;
-    for (int j = 0; j < k; ++j)
-      y = fmaf(gate[(size_t)m * k + j], yE[((size_t)(f * maxB + b) * k + j) * d + n], y);
+    for (int j = 0; j < kr; ++j)
+      y = fmaf(gate[(size_t)m * ka + j], yE[((size_t)(f * maxB + b) * ka + j) * d + n], y);
     if (f) {
       float y1;
       if (C.saved) {
         y1 = C.y1s[(size_t)b * d + n];
       } else {
         y1 = 0.f;
-        for (int j = 0; j < k; ++j) y1 = fmaf(gate[(size_t)b * k + j], yE[((size_t)b * k + j) * d + n], y1);
+        for (int j = 0; j < k; ++j) y1 = fmaf(gate[(size_t)b * ka + j], yE[((size_t)b * ka + j) * d + n], y1);
       }
       y = fmaf(cvec[n], y1, y);
     } else if (C.save) {
@@ -1021,7 +1067,8 @@ void launch_moe_combine(const Dims& D, const Buffers& Bf, const float* cvec, con
                         cudaStream_t s) {
   int n = R.hi - R.lo;
   if (n <= 0) return;
-  launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, s, Bf.yE, Bf.gate, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.maxB);
+  launch_pdl(k_moe_combine, dim3(n), dim3(256), 0, s, Bf.yE, Bf.gate, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.ka,
+             D.maxB);
 }
 
 }  // namespace df

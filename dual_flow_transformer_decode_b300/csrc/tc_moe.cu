@@ -42,6 +42,7 @@ struct MoeArgs {
   float* yE;          // [E][nxe][d]
   Ctrl* ctrl;
   int maxB, k, E, Fe, d, nxe;
+  int B;          // batch: entries below B*k are replayed, the others auxiliary-own
   int prim, aux;  // active flows
   int op;         // 0: gate/up, 1: down
   int tiles;      // 128-row weight tiles per expert
@@ -156,15 +157,16 @@ __global__ void __launch_bounds__(128, 1)
         const int i = u / 64, p = u % 64;
         const int fi = tile * 64 + p;
         const int ent = a.elist[(size_t)e * a.maxB + i];
+        const bool own = ent >= a.B * a.k;  // auxiliary-own expert: no primary partner, no b coupling
         const float* r1 = st + (2 * i) * kBM;
         const float* r2 = st + (2 * i + 1) * kBM;
         const float z1 = silu_f(r1[p]) * r1[p + 64];
-        if (a.prim) {
+        if (a.prim && !own) {
           if (a.C.save) a.C.z1s[(size_t)ent * a.Fe + fi] = z1;
           a.zE[((size_t)e * a.nxe + 2 * i) * a.Fe + fi] = __float2bfloat16_rn(z1);
         }
         if (a.aux) {
-          const float zp = a.C.saved ? a.C.z1s[(size_t)ent * a.Fe + fi] : z1;
+          const float zp = own ? 0.f : a.C.saved ? a.C.z1s[(size_t)ent * a.Fe + fi] : z1;
           const float z2 = fmaf(a.bvec[fi], zp, silu_f(r2[p]) * r2[p + 64]);
           a.zE[((size_t)e * a.nxe + 2 * i + 1) * a.Fe + fi] = __float2bfloat16_rn(z2);
         }
@@ -188,15 +190,28 @@ __global__ void __launch_bounds__(128, 1)
 // row 2i+1 <- auxiliary row of entry i.
 __global__ void k_moe_gather(const __nv_bfloat16* __restrict__ u, const int* __restrict__ ecount,
                              const int* __restrict__ elist, __nv_bfloat16* __restrict__ xg, int B, int d, int k,
-                             int maxB, int nxe) {
+                             int ka, int maxB, int nxe) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int e = blockIdx.x, slot = blockIdx.y;
   if (slot >= 2 * ecount[e]) return;
   const int ent = elist[(size_t)e * maxB + slot / 2];
-  const int b = ent / k, f = slot & 1;
-  const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)(f * B + b) * d);
+  const int f = slot & 1;
   uint4* dst = reinterpret_cast<uint4*>(xg + ((size_t)e * nxe + slot) * d);
+  if (ent >= B * k) {
+    // auxiliary-own entry: only the auxiliary row exists; the primary slot
+    // is zero, so its SwiGLU output, and the b coupling it feeds, is zero
+    const int b = (ent - B * k) / (ka - k);
+    if (f == 0) {
+      for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)(B + b) * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+    return;
+  }
+  const int b = ent / k;
+  const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)(f * B + b) * d);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
 }
 
@@ -206,26 +221,32 @@ __global__ void k_moe_gather(const __nv_bfloat16* __restrict__ u, const int* __r
 constexpr int kCombineMaxK = 16;
 
 __global__ void k_moe_combine_tc(const float* __restrict__ yE, const float* __restrict__ gate,
-                                 const int* __restrict__ topk_l, const int* __restrict__ eslot,
-                                 const float* __restrict__ cvec, float* __restrict__ h, Couple C, int B, int lo,
-                                 int d, int k, int nxe) {
+                                 const int* __restrict__ topk_l, const int* __restrict__ topkx,
+                                 const int* __restrict__ eslot, const float* __restrict__ cvec,
+                                 float* __restrict__ h, Couple C, int B, int lo, int d, int k, int ka, int nxe) {
   __shared__ size_t ofs[kCombineMaxK];  // start of the primary row of entry j in yE
   __shared__ float g_own[kCombineMaxK], g_prim[kCombineMaxK];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int m = lo + blockIdx.x;
   const int f = m >= B, b = m - f * B;
-  if (threadIdx.x < k) {
+  const int kr = f ? ka : k;  // entries of this row: the replayed ones, then the auxiliary-own ones
+  if (threadIdx.x < kr) {
     const int j = threadIdx.x;
-    ofs[j] = ((size_t)topk_l[b * k + j] * nxe + 2 * eslot[b * k + j]) * d;
-    g_own[j] = gate[(size_t)m * k + j];
-    g_prim[j] = gate[(size_t)b * k + j];
+    if (j < k) {
+      ofs[j] = ((size_t)topk_l[b * k + j] * nxe + 2 * eslot[b * k + j]) * d;
+      g_prim[j] = gate[(size_t)b * ka + j];
+    } else {
+      const int jx = j - k, ent = B * k + b * (ka - k) + jx;
+      ofs[j] = ((size_t)topkx[b * (ka - k) + jx] * nxe + 2 * eslot[ent]) * d;
+    }
+    g_own[j] = gate[(size_t)m * ka + j];
   }
   __syncthreads();
   const int n = blockIdx.y * blockDim.x + threadIdx.x;
   if (n >= d) return;
   float y = 0.f;
-  for (int j = 0; j < k; ++j) y = fmaf(g_own[j], yE[ofs[j] + (size_t)f * d + n], y);
+  for (int j = 0; j < kr; ++j) y = fmaf(g_own[j], yE[ofs[j] + (size_t)f * d + n], y);
   if (f) {
     float y1;
     if (C.saved) {
@@ -309,7 +330,7 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
                     const float* cvec, const Couple& C, const Rows& R, cudaStream_t s) {
   const int prim = R.has_primary(), aux = R.has_aux();
   launch_pdl(k_moe_gather, dim3(D.E, P.nxe), dim3(128), 0, s, (const __nv_bfloat16*)Bf.u, (const int*)Bf.ecount,
-             (const int*)Bf.elist, (__nv_bfloat16*)Bf.xg, R.B, D.d, D.k, D.maxB, P.nxe);
+             (const int*)Bf.elist, (__nv_bfloat16*)Bf.xg, R.B, D.d, D.k, D.ka, D.maxB, P.nxe);
   MoeArgs a{};
   a.ecount = Bf.ecount;
   a.elist = Bf.elist;
@@ -320,6 +341,7 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
   a.ctrl = Bf.ctrl;
   a.maxB = D.maxB;
   a.k = D.k;
+  a.B = R.B;
   a.E = D.E;
   a.Fe = D.Fe;
   a.d = D.d;
@@ -335,8 +357,9 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
   a.rows_w = D.d;
   launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe), s, P.w_d[layer], P.x_z, D.Fe, a);
   const int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt, (const float*)Bf.gate,
-             topk_l, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, P.nxe);
+  launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt,
+             (const float*)Bf.gate, topk_l, (const int*)Bf.topkx, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo,
+             D.d, D.k, D.ka, P.nxe);
 }
 
 }  // namespace df

@@ -60,6 +60,12 @@ typedef struct {
   float rope_theta, norm_eps;
   int dtype;               /* df_dtype */
   int max_batch, max_len;  /* capacity of the KV cache and workspace        */
+  int aux_top_k;           /* MoE: experts per token of the auxiliary flow:
+                              the primary's top_k (replayed) plus
+                              aux_top_k - top_k chosen from its own router
+                              logits among the other experts (0 = top_k).
+                              Prefill cost is unchanged; decode reads the
+                              extra experts' weights once for the batch.   */
 } df_config;
 
 /* Parameter set (all device pointers; the struct and its per-layer arrays
@@ -158,8 +164,11 @@ df_status df_set_mode(df_ctx* ctx, int aux_on, int ungrouped);
 
 /* Optional per-step diagnostics written by later decode steps (device
  * pointers, each may be NULL): logp1, logp2 fp32 [B][vocab]; topk int32
- * [n_layers][B][top_k] (MoE primary expert indices, descending router
- * logit); router fp32 [n_layers][B][n_experts] (primary router logits). */
+ * [n_layers][B][k] with k = max(top_k, aux_top_k): entries 0..top_k-1 are
+ * the primary experts (descending router logit), entries top_k..k-1 the
+ * auxiliary flow's own experts (descending auxiliary router logit; written
+ * only while the auxiliary flow runs); router fp32 [n_layers][B][n_experts]
+ * (primary router logits). */
 df_status df_debug_outputs(df_ctx* ctx, float* logp1, float* logp2, int32_t* topk, float* router);
 
 /* Decode step without workspace scratch for the attention partials.

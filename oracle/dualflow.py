@@ -385,6 +385,7 @@ class Oracle:
             nxa = max(cfg.aux_k - cfg.top_k, 0) if cfg.is_moe else 0
             aux_extra = np.zeros((L, self.nb, nxa), dtype=np.int64)
             aux_margin = np.full((L, self.nb), np.inf)
+            router2 = []
             tr = []
             for l in range(L):
                 sv = saved[l]
@@ -398,6 +399,7 @@ class Oracle:
                 h2_attn = h2.copy()
                 if cfg.is_moe:
                     r2 = self._router(l, h2)
+                    router2.append(r2)
                     u2 = self.q(rmsnorm(h2, self.W(l, "mlp_norm"), cfg.norm_eps))
                     y2 = np.zeros_like(h2)
                     nx = cfg.aux_k - cfg.top_k
@@ -433,6 +435,7 @@ class Oracle:
             if cfg.is_moe:
                 out["topk_aux"] = aux_extra
                 out["topk_aux_margin"] = aux_margin
+                out["router2"] = np.stack(router2)
             out["logp_mix"] = mix
             out["alpha"] = alpha
             out["argmax"] = np.argmax(mix, axis=1)

@@ -44,7 +44,8 @@ class GpuRun:
         al = torch.zeros(B, device=dev)
         l1 = torch.zeros(B, V, device=dev)
         l2 = torch.zeros(B, V, device=dev)
-        tk = torch.zeros(cfg.n_layers, B, max(cfg.top_k, 1), dtype=torch.int32, device=dev)
+        ka = max(cfg.aux_k, cfg.top_k, 1)  # replayed experts, then the auxiliary flow's own
+        tk = torch.zeros(cfg.n_layers, B, ka, dtype=torch.int32, device=dev)
         rl = torch.zeros(cfg.n_layers, B, max(cfg.n_experts, 1), device=dev)
         if debug:
             self.m.debug_outputs(l1, l2 if aux else None, tk if cfg.n_experts else None,
@@ -66,7 +67,10 @@ class GpuRun:
             if aux:
                 r["logp2"] = l2.double().cpu().numpy()
             if cfg.n_experts:
-                r["topk"] = tk.cpu().numpy().astype(np.int64)
+                tkh = tk.cpu().numpy().astype(np.int64)
+                r["topk"] = tkh[:, :, :cfg.top_k]
+                if aux and cfg.aux_k > cfg.top_k:
+                    r["topk_aux"] = tkh[:, :, cfg.top_k:cfg.aux_k]
                 r["router1"] = rl.double().cpu().numpy()
             self.steps.append(r)
         if keep_kv:
@@ -167,6 +171,25 @@ def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
                     elif set(gs.tolist()) != set(os_.tolist()):
                         rep["topk_mismatch"].append((s, l, i, gs.tolist(), os_.tolist(),
                                                      float(o["topk_margin"][l, i]), eps))
+                    if "topk_aux" in g and "topk_aux" in o and set(gs.tolist()) == set(os_.tolist()):
+                        # the auxiliary flow's own experts rank its own router
+                        # logits, which the library does not export; their
+                        # deviation is bounded here by twice the primary row's
+                        # (the auxiliary rows carry the primary's deviations
+                        # through the couplings).  A primary near tie that
+                        # went the other way changes the set they exclude, so
+                        # they are compared only where the replayed sets agree.
+                        eps2 = 2 * eps
+                        rep["decisions"] += 1
+                        gx, ox = g["topk_aux"][l, b], o["topk_aux"][l, i]
+                        if o["topk_aux_margin"][l, i] <= 2 * eps2:
+                            rep["near_ties"].append(("topk_aux", s, l, i, float(o["topk_aux_margin"][l, i]), eps2))
+                            r2 = o["router2"][l][i]
+                            if r2[ox].min() - r2[gx].min() > 2 * eps2:
+                                rep["invalid_near_ties"].append(("topk_aux", s, l, i, gx.tolist(), ox.tolist()))
+                        elif set(gx.tolist()) != set(ox.tolist()):
+                            rep["topk_mismatch"].append(("aux", s, l, i, gx.tolist(), ox.tolist(),
+                                                         float(o["topk_aux_margin"][l, i]), eps2))
     rep["tol"] = tol
     return rep
 
