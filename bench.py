@@ -291,17 +291,20 @@ def run_ours(args, rank, world, local_rank):
         return {"metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
                 "quick": True, "config": {"workload": cfg.name}, "kernels_per_step": kernels, "clocks": clk}
 
-    # MoE: the experts a step actually reads, per layer (union of the primary
-    # top-k sets over the batch), from the routing of one step at t_mid
-    moe_union = None
+    # MoE: the experts a step actually reads, per layer, from the routing of
+    # one step at t_mid: the union over the batch of the primary top-k sets
+    # and of the auxiliary flow's own experts (when it has any)
+    moe_union = moe_union_primary = None
     if cfg.n_experts:
-        tk = torch.zeros(cfg.n_layers, B, cfg.top_k, dtype=torch.int32, device=dev)
+        ka = max(cfg.aux_k, cfg.top_k)
+        tk = torch.zeros(cfg.n_layers, B, ka, dtype=torch.int32, device=dev)
         model.debug_outputs(topk=tk)
         model.set_length(B, t_mid)
         step(0)
         model.sync()
         tkh = tk.cpu().numpy()
         moe_union = float(np.mean([len(np.unique(tkh[l])) for l in range(cfg.n_layers)]))
+        moe_union_primary = float(np.mean([len(np.unique(tkh[l, :, :cfg.top_k])) for l in range(cfg.n_layers)]))
         model.debug_outputs()
 
     # per-step latency distribution: an event pair around every step
@@ -328,9 +331,11 @@ def run_ours(args, rank, world, local_rank):
         kk = min(K, 32)
         ms = max_over_ranks(timed(min(W, 3), kk)) / kk
         abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1),
-                     # two passes each read every weight and the whole cache; primary-only reads them once
-                     "algorithmic_bytes": 2 * step_bytes(cfg, B, t_mid, moe_union) if ung
-                     else step_bytes(cfg, B, t_mid, moe_union)}
+                     # two passes each read every weight and the whole cache (the
+                     # auxiliary pass its own experts too); primary-only reads them once
+                     "algorithmic_bytes": step_bytes(cfg, B, t_mid, moe_union_primary) +
+                     step_bytes(cfg, B, t_mid, moe_union) if ung
+                     else step_bytes(cfg, B, t_mid, moe_union_primary)}
     model.set_mode(1, 0)
 
     # dominant operation: time every op, cycling layers, with CUDA events
@@ -388,6 +393,7 @@ def run_ours(args, rank, world, local_rank):
         "step_latency": latency,
         "prefill": prefill,
         "moe_experts_read_per_layer": moe_union,
+        "moe_experts_read_per_layer_primary": moe_union_primary,
         "ablation": abl,
         "e2e": e2e,
         "gpu_launches": kernels * K if kernels >= 0 else None,
