@@ -338,6 +338,28 @@ def run_ours(args, rank, world, local_rank):
                      else step_bytes(cfg, B, t_mid, moe_union_primary)}
     model.set_mode(1, 0)
 
+    # generation: the same positions, each step fed the token drawn from
+    # p_mix at the step before (one df_generate call for all K steps)
+    gen_out = torch.empty(max(K, 3), B, dtype=torch.int32, device=dev)
+    tok_buf.copy_(steps_tok[0])
+    model.set_length(B, P)
+    model.generate(tok_buf, min(W, 3), args.seed, gen_out)  # warm-up (captures the step graph)
+    model.set_length(B, P)
+    tok_buf.copy_(steps_tok[0])
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    model.generate(tok_buf, K, args.seed, gen_out)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    gms = max_over_ranks(g0.elapsed_time(g1)) / K
+    generation = {"ms_per_step": round(gms, 4), "tokens_per_s": round(world * B / (gms / 1e3), 1),
+                  "steps": K, "draw": "Gumbel-max over Philox4x64-10 noise, fed back on the device"}
+
     # dominant operation: time every op, cycling layers, with CUDA events
     model.set_length(B, t_mid)
     step(0)
@@ -395,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
         "moe_experts_read_per_layer": moe_union,
         "moe_experts_read_per_layer_primary": moe_union_primary,
         "ablation": abl,
+        "generation": generation,
         "e2e": e2e,
         "gpu_launches": kernels * K if kernels >= 0 else None,
         "kernels_per_step": kernels,

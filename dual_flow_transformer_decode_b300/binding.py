@@ -45,7 +45,8 @@ _lib = None
 
 EXPORTS = ["df_workspace_bytes", "df_create", "df_prefill", "df_set_length", "df_decode_step",
            "df_decode_step_host", "df_set_mode", "df_debug_outputs", "df_sync", "df_length",
-           "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc"]
+           "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc",
+           "df_generate"]
 
 DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6, "layers": 7}
 
@@ -70,6 +71,8 @@ def lib():
     L.df_decode_step.restype = i
     L.df_decode_step_noalloc.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step_noalloc.restype = i
+    L.df_generate.argtypes = [vp, vp, i, C.c_ulonglong, vp, vp]
+    L.df_generate.restype = i
     L.df_decode_step_host.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step_host.restype = i
     L.df_set_mode.argtypes = [vp, i, i]
@@ -140,6 +143,12 @@ def df_decode_step_noalloc(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_p
     check(ctx, lib().df_decode_step_noalloc(ctx, C.c_void_p(tokens_ptr), C.c_void_p(logp_mix_ptr or None),
                                             C.c_void_p(argmax_ptr or None), C.c_void_p(alpha_ptr or None)),
           "df_decode_step_noalloc")
+
+
+def df_generate(ctx, tokens_ptr: int, n_steps: int, seed: int, out_tokens_ptr: int, logp_mix_ptr: int = 0) -> None:
+    check(ctx, lib().df_generate(ctx, C.c_void_p(tokens_ptr or None), n_steps, C.c_ulonglong(seed & (2 ** 64 - 1)),
+                                 C.c_void_p(out_tokens_ptr or None), C.c_void_p(logp_mix_ptr or None)),
+          "df_generate")
 
 
 def df_decode_step_host(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_ptr: int = 0,

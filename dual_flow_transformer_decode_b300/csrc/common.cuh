@@ -16,11 +16,49 @@ struct Ctrl {
   int err;        // first latched device error (0 = none)
   int err_info;   // kernel-specific detail for the first error
   int mk_abort;   // set by a persistent-kernel CTA that gave up; the others stop waiting
-  int pad[60];
+  unsigned long long seed;  // key of the sampling noise (generation)
+  int pad[58];
 };
+static_assert(sizeof(Ctrl) == 256, "control block layout");
 
 __device__ __forceinline__ void latch_error(Ctrl* c, int code, int info) {
   if (atomicCAS(&c->err, 0, code) == 0) c->err_info = info;
+}
+
+// Philox4x64 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): a keyed bijection of a 256-bit
+// counter.  Each round multiplies counter words 0 and 2 by two fixed odd
+// constants and mixes each product's high half into the other two words and
+// the key; the key advances by two Weyl increments between rounds.
+struct Philox4x64Out {
+  unsigned long long w[4];
+};
+__device__ __forceinline__ Philox4x64Out philox4x64_10(unsigned long long c0, unsigned long long c1,
+                                                       unsigned long long c2, unsigned long long c3,
+                                                       unsigned long long k0, unsigned long long k1) {
+  constexpr unsigned long long kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
+  constexpr unsigned long long kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long lo0 = kM0 * c0, hi0 = __umul64hi(kM0, c0);
+    const unsigned long long lo1 = kM1 * c2, hi1 = __umul64hi(kM1, c2);
+    const unsigned long long n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += kW0;
+    k1 += kW1;
+  }
+  return Philox4x64Out{{c0, c1, c2, c3}};
+}
+
+// Standard Gumbel noise from one 64-bit word: u = (2·(w >> 41) + 1)·2^-24, an
+// odd multiple of 2^-24 strictly inside (0, 1) and exact in fp32;
+// g = -log(-log u).
+__device__ __forceinline__ float gumbel_of_word(unsigned long long w) {
+  const float u = (float)(2u * (unsigned)(w >> 41) + 1u) * 0x1p-24f;
+  return -logf(-logf(u));
 }
 
 template <typename T> struct Num;

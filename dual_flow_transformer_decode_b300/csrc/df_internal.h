@@ -78,6 +78,8 @@ struct Buffers {
   float* out_logp;  // [maxB][V] host-step staging
   int* out_arg;     // [maxB]
   float* out_alpha; // [maxB]
+  int* gen_tok;     // [maxB] generation: the next step's input tokens (written by the draw)
+  int* gen_hist;    // [max_len][maxB] generation: the token drawn at each position
   float* rope;      // [max_len][hd/2][2] cos, sin
   int* tickets;     // split-K tile tickets
   int* attn_tickets;  // [maxB][Hkv] split-merge tickets of the attention kernel
@@ -113,6 +115,7 @@ struct Couple {
 void kernels_init();   // one-time function attributes (dynamic shared memory limits)
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s);
 void launch_advance_pos(Ctrl* c, cudaStream_t s);
+void launch_set_seed(Ctrl* c, unsigned long long seed, cudaStream_t s);
 void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void* emb2,
                   const int32_t* tokens, int tok_stride, int use_pos, const Rows& R, cudaStream_t s);
 void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out, float* out_f32,
@@ -142,8 +145,12 @@ void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, 
 void launch_attn_combine(const Dims& D, const Buffers& Bf, int splits, const Rows& R, cudaStream_t s);
 
 // Softmax / mixture / argmax.
+// Softmax of both flows, mixture, log p_mix and its argmax; with sample_tok
+// set, also one draw from p_mix per sequence (written to sample_tok[b] and,
+// if set, to sample_hist[t][b], row stride maxB).
 void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax,
-                float* alpha, float* logp1, float* logp2, cudaStream_t s);
+                float* alpha, float* logp1, float* logp2, int32_t* sample_tok, int32_t* sample_hist,
+                cudaStream_t s);
 
 // MoE with router replay.
 void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s);

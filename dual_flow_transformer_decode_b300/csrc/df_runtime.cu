@@ -83,6 +83,7 @@ struct df_ctx {
   int force_generic = 0;
   GraphSlot dec, pre;
   GraphSlot dec_static;  // graph of df_decode_step_noalloc
+  GraphSlot gen;         // graph of one df_generate step
   int last_kernels = -1;
   df::TcPlan tc;
   df::MoePlan moe;
@@ -218,6 +219,8 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.out_logp = (float*)take((size_t)D.maxB * D.V * 4);
   b.out_arg = (int*)take(D.maxB * 4);
   b.out_alpha = (float*)take(D.maxB * 4);
+  b.gen_tok = (int*)take(D.maxB * 4);
+  b.gen_hist = (int*)take((size_t)D.max_len * D.maxB * 4);
   b.rope = (float*)take((size_t)D.max_len * D.hd * 4);
   b.tickets_cap = df::tc_tickets_needed(D);
   b.tickets = (int*)take(b.tickets_cap * 4);
@@ -242,6 +245,8 @@ struct StepOut {
   float* logp_mix;
   int32_t* argmax;
   float* alpha;
+  int32_t* sample_tok = nullptr;   // generation: the drawn tokens, the next step's input
+  int32_t* sample_hist = nullptr;  // generation: [max_len][maxB] history of draws
 };
 
 Couple layer_couple(df_ctx* X, int l, int save, int saved) {
@@ -388,7 +393,7 @@ void enqueue_decode(df_ctx* X, const int32_t* tokens, const StepOut& o) {
     enqueue_pass(X, both, 0, 0, true);
   }
   df::launch_mix(D, X->Bf, B, X->aux_on, o.logp_mix, o.argmax, o.alpha, X->dbg_logp1, X->aux_on ? X->dbg_logp2 : nullptr,
-                 s);
+                 o.sample_tok, o.sample_hist, s);
   df::launch_advance_pos(X->Bf.ctrl, s);
 }
 
@@ -567,6 +572,7 @@ static df_status set_batch(df_ctx* X, int B) {
     X->dec.reset();
     X->pre.reset();
     X->dec_static.reset();
+    X->gen.reset();
     X->B = B;
     X->splits = df::attn_splits(X->D, B);
     std::string perr;
@@ -645,6 +651,41 @@ df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int3
   df_status st = run_captured(X, X->dec, key, [&] { enqueue_decode(X, tokens, o); }, 1);
   if (st != DF_OK) return st;
   X->t += 1;
+  return DF_OK;
+}
+
+df_status df_generate(df_ctx* X, const int32_t* tokens, int n_steps, unsigned long long seed, int32_t* out_tokens,
+                      float* logp_mix) {
+  if (!X) return DF_ERR_ARG;
+  if (n_steps < 0) return fail(X, DF_ERR_ARG, "df_generate: n_steps < 0");
+  if (n_steps > 0 && (!tokens || !out_tokens)) return fail(X, DF_ERR_ARG, "df_generate: null tokens or out_tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_generate before df_prefill");
+  if (n_steps > X->cfg.max_len - X->t) return fail(X, DF_ERR_CAPACITY, "df_generate: t + n_steps > max_len");
+  if (n_steps == 0) return DF_OK;
+  const int B = X->B, t0 = X->t;
+  cudaError_t e = cudaSuccess;
+  if (tokens != X->Bf.gen_tok)
+    e = cudaMemcpyAsync(X->Bf.gen_tok, tokens, (size_t)B * 4, cudaMemcpyDeviceToDevice, X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_generate: token copy");
+  df::launch_set_seed(X->Bf.ctrl, seed, X->stream);
+  GraphKey key{};
+  key.p[0] = X->Bf.gen_tok;
+  key.p[1] = logp_mix;
+  key.p[4] = X->dbg_logp1;
+  key.p[5] = X->dbg_logp2;
+  key.p[6] = X->dbg_topk;
+  key.p[7] = X->dbg_router;
+  key.i[0] = X->aux_on;
+  key.i[1] = X->ungrouped;
+  key.i[2] = B;
+  key.i[3] = X->force_generic;
+  StepOut o{logp_mix, nullptr, nullptr, X->Bf.gen_tok, X->Bf.gen_hist};
+  df_status st = run_captured(X, X->gen, key, [&] { enqueue_decode(X, X->Bf.gen_tok, o); }, n_steps);
+  if (st != DF_OK) return st;
+  X->t += n_steps;
+  e = cudaMemcpy2DAsync(out_tokens, (size_t)B * 4, X->Bf.gen_hist + (size_t)t0 * X->D.maxB, (size_t)X->D.maxB * 4,
+                        (size_t)B * 4, n_steps, cudaMemcpyDeviceToDevice, X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_generate: output copy");
   return DF_OK;
 }
 
@@ -756,6 +797,7 @@ void df_destroy(df_ctx* X) {
   X->dec.reset();
   X->pre.reset();
   X->dec_static.reset();
+  X->gen.reset();
   df::tc_plan_free(X->tc);
   df::moe_tc_free(X->moe);
   df::attn_fast_free(X->at);

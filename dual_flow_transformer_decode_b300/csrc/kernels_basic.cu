@@ -32,6 +32,11 @@ __global__ void k_advance_pos(Ctrl* c) {
   ptx::grid_dep_launch();
   c->t += 1;
 }
+__global__ void k_set_seed(Ctrl* c, unsigned long long seed) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  c->seed = seed;
+}
 
 template <typename T>
 __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
@@ -64,6 +69,9 @@ void kernels_init() {
 
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { launch_pdl(k_set_pos, dim3(1), dim3(1), 0, s, c, t); }
 void launch_advance_pos(Ctrl* c, cudaStream_t s) { launch_pdl(k_advance_pos, dim3(1), dim3(1), 0, s, c); }
+void launch_set_seed(Ctrl* c, unsigned long long seed, cudaStream_t s) {
+  launch_pdl(k_set_seed, dim3(1), dim3(1), 0, s, c, seed);
+}
 
 // ------------------------------------------------------------------ embedding
 // h[b] = E1[x_b], h[B+b] = E2[x_b]: the two flows use separate token
@@ -625,10 +633,21 @@ __device__ __forceinline__ void argmax_merge(float& best, int& bi, float ov, int
   }
 }
 
+// One CTA cluster per sequence b; CTA r of the cluster owns the vocabulary
+// chunk [v0, v1).  Pass 1 forms the online (max, Σe, Σe²) statistics of both
+// flows' logits, merged over the cluster in rank order.  Pass 2 walks the
+// chunk in blocks of 4 tokens (block j holds tokens 4j..4j+3 and belongs to
+// the CTA whose chunk holds 4j) and writes log p_mix, tracking its argmax;
+// when sampling, the same pass adds one Philox4x64-10 block of Gumbel noise
+// per 4 tokens (counter (j, b, t, 0), key (seed, 0)) and tracks the argmax of
+// log p_mix + g: one draw from p_mix (Gumbel-max), written to sample_tok[b]
+// (the next step's input) and to sample_hist[t][b].
 __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ logits, int B, int V, int aux_on,
                                                      float* __restrict__ logp_mix, int32_t* __restrict__ argmax,
                                                      float* __restrict__ alpha_out, float* __restrict__ logp1,
-                                                     float* __restrict__ logp2) {
+                                                     float* __restrict__ logp2, const Ctrl* __restrict__ ctrl,
+                                                     int32_t* __restrict__ sample_tok,
+                                                     int32_t* __restrict__ sample_hist, int hist_stride) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   __shared__ MixStat wstat[kMixThreads / 32];
@@ -637,6 +656,10 @@ __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ l
   __shared__ int cidx;
   __shared__ float wbest[kMixThreads / 32];
   __shared__ int widx[kMixThreads / 32];
+  __shared__ float csbest;
+  __shared__ int csidx;
+  __shared__ float wsbest[kMixThreads / 32];
+  __shared__ int wsidx[kMixThreads / 32];
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int b = blockIdx.y;
@@ -679,50 +702,84 @@ __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ l
   const float alpha = aux_on ? 0.5f + 0.5f * coll : 1.0f;
   const float la = logf(alpha);
   const float lb = (alpha < 1.0f) ? log1pf(-alpha) : -INFINITY;
-  float best = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int v = v0 + threadIdx.x; v < v1; v += kMixThreads) {
-    const float lp1 = l1[v] - lse1;
-    float lm = lp1;
-    if (aux_on) {
-      const float lp2 = l2[v] - lse2;
-      lm = logaddexp_f(la + lp1, lb + lp2);
-      if (logp2) logp2[(size_t)b * V + v] = lp2;
-    }
-    if (logp1) logp1[(size_t)b * V + v] = lp1;
-    if (logp_mix) logp_mix[(size_t)b * V + v] = lm;
-    if (lm > best) {
-      best = lm;
-      bi = v;
+  const bool samp = sample_tok != nullptr;
+  const unsigned long long seed = samp ? ctrl->seed : 0ull;
+  const int tpos = samp ? ctrl->t : 0;
+  float best = -INFINITY, sbest = -INFINITY;
+  int bi = 0x7fffffff, sbi = 0x7fffffff;
+  const int jb0 = (v0 + 3) >> 2, jb1 = (v1 + 3) >> 2;
+  for (int j = jb0 + threadIdx.x; j < jb1; j += kMixThreads) {
+    Philox4x64Out noise{};
+    if (samp) noise = philox4x64_10((unsigned long long)j, (unsigned long long)b, (unsigned long long)tpos, 0ull, seed, 0ull);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int v = 4 * j + e;
+      if (v >= V) break;
+      const float lp1 = l1[v] - lse1;
+      float lm = lp1;
+      if (aux_on) {
+        const float lp2 = l2[v] - lse2;
+        lm = logaddexp_f(la + lp1, lb + lp2);
+        if (logp2) logp2[(size_t)b * V + v] = lp2;
+      }
+      if (logp1) logp1[(size_t)b * V + v] = lp1;
+      if (logp_mix) logp_mix[(size_t)b * V + v] = lm;
+      if (lm > best) {
+        best = lm;
+        bi = v;
+      }
+      if (samp) {
+        const float key = lm + gumbel_of_word(noise.w[e]);
+        if (key > sbest) {
+          sbest = key;
+          sbi = v;
+        }
+      }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int o = 16; o > 0; o >>= 1) {
     argmax_merge(best, bi, __shfl_xor_sync(0xffffffffu, best, o), __shfl_xor_sync(0xffffffffu, bi, o));
+    argmax_merge(sbest, sbi, __shfl_xor_sync(0xffffffffu, sbest, o), __shfl_xor_sync(0xffffffffu, sbi, o));
+  }
   if (lane == 0) {
     wbest[w] = best;
     widx[w] = bi;
+    wsbest[w] = sbest;
+    wsidx[w] = sbi;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 1; i < kMixThreads / 32; ++i) argmax_merge(best, bi, wbest[i], widx[i]);
+    for (int i = 1; i < kMixThreads / 32; ++i) {
+      argmax_merge(best, bi, wbest[i], widx[i]);
+      argmax_merge(sbest, sbi, wsbest[i], wsidx[i]);
+    }
     cbest = best;
     cidx = bi;
+    csbest = sbest;
+    csidx = sbi;
   }
   cl.sync();
   if (r == 0 && threadIdx.x == 0) {
-    float cb = cbest;
-    int ci = cidx;
-    for (int i = 1; i < kMixCl; ++i) argmax_merge(cb, ci, *cl.map_shared_rank(&cbest, i), *cl.map_shared_rank(&cidx, i));
+    float cb = cbest, sb = csbest;
+    int ci = cidx, si = csidx;
+    for (int i = 1; i < kMixCl; ++i) {
+      argmax_merge(cb, ci, *cl.map_shared_rank(&cbest, i), *cl.map_shared_rank(&cidx, i));
+      argmax_merge(sb, si, *cl.map_shared_rank(&csbest, i), *cl.map_shared_rank(&csidx, i));
+    }
     if (argmax) argmax[b] = ci;
     if (alpha_out) alpha_out[b] = alpha;
+    if (samp) {
+      sample_tok[b] = si;
+      if (sample_hist) sample_hist[(size_t)tpos * hist_stride + b] = si;
+    }
   }
   // keep every CTA's shared memory alive until rank 0 has read it
   cl.sync();
 }
 
 void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp_mix, int32_t* argmax, float* alpha,
-                float* logp1, float* logp2, cudaStream_t s) {
+                float* logp1, float* logp2, int32_t* sample_tok, int32_t* sample_hist, cudaStream_t s) {
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(kMixCl, B);
   lc.blockDim = dim3(kMixThreads);
@@ -737,7 +794,8 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
   at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   lc.attrs = at;
   lc.numAttrs = 2;
-  cudaLaunchKernelEx(&lc, k_mix, (const float*)Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2);
+  cudaLaunchKernelEx(&lc, k_mix, (const float*)Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2,
+                     (const Ctrl*)Bf.ctrl, sample_tok, sample_hist, D.maxB);
 }
 
 // ------------------------------------------------------------------ MoE (router replay)

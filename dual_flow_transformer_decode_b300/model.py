@@ -109,6 +109,17 @@ class DualFlowModel:
                           argmax.data_ptr() if argmax is not None else 0,
                           alpha.data_ptr() if alpha is not None else 0)
 
+    def generate(self, tokens: torch.Tensor, n_steps: int, seed: int, out_tokens: torch.Tensor,
+                 logp_mix: torch.Tensor | None = None) -> None:
+        """n_steps decode steps, each fed the token drawn from p_mix at the
+        step before (tokens feeds the first); out_tokens int32 [n_steps][B]
+        receives the draws, logp_mix (optional) the last step's log p_mix."""
+        assert tokens.dtype == torch.int32 and tokens.is_cuda
+        assert out_tokens.dtype == torch.int32 and out_tokens.is_cuda and out_tokens.is_contiguous()
+        assert out_tokens.numel() >= n_steps * tokens.numel()
+        _b.df_generate(self.ctx, tokens.data_ptr(), n_steps, seed, out_tokens.data_ptr(),
+                       logp_mix.data_ptr() if logp_mix is not None else 0)
+
     def decode_step_host(self, tokens: torch.Tensor, logp_mix: torch.Tensor | None = None,
                          argmax: torch.Tensor | None = None, alpha: torch.Tensor | None = None) -> None:
         assert tokens.dtype == torch.int32 and not tokens.is_cuda

@@ -154,6 +154,27 @@ df_status df_decode_step(df_ctx* ctx, const int32_t* tokens, float* logp_mix, in
 df_status df_decode_step_host(df_ctx* ctx, const int32_t* tokens, float* logp_mix,
                               int32_t* argmax, float* alpha);
 
+/* Generation: n_steps decode steps on the device, each fed the token drawn
+ * from p_mix at the step before ("Problema Central": decode generates tokens
+ * one at a time; "Mecanismos Clave", Objetivo de Mezcla: p_mix is the
+ * next-token distribution).  The first step is fed tokens (device int32
+ * [B]); the step at position t draws, for sequence b,
+ *     x = argmax_v ( log p_mix[v] + g_v ),  g_v = -log(-log u_v)
+ * (Gumbel-max: one draw from p_mix itself, no temperature or truncation;
+ * lowest index among equal maxima), with u_v = (2*(w >> 41) + 1) / 2^24 and
+ * w word (v mod 4) of Philox4x64-10 (Salmon et al., SC 2011) at counter
+ * (v div 4, b, t, 0) and key (seed, 0).  A draw therefore depends only on
+ * (seed, t, b, p_mix).
+ * Outputs (device): out_tokens int32 [n_steps][B], the token drawn at each
+ * step (row s is the input of step s+1); logp_mix fp32 [B][vocab] or NULL,
+ * the last step's log p_mix.  The debug outputs and the mode (aux_on,
+ * ungrouped) apply as for df_decode_step; with aux_on = 0 the draw is from
+ * p1.  Advances the position by n_steps.  DF_ERR_CAPACITY (nothing enqueued)
+ * if t + n_steps > max_len; n_steps = 0 does nothing.  tokens may alias
+ * out_tokens of an earlier call (it is copied before the first step). */
+df_status df_generate(df_ctx* ctx, const int32_t* tokens, int n_steps, unsigned long long seed,
+                      int32_t* out_tokens, float* logp_mix);
+
 /* Execution mode for later decode steps.
  *  aux_on = 0: standard decode (primary flow only); logp_mix receives
  *              log p1, alpha receives 1.
