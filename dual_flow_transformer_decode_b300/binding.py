@@ -23,7 +23,8 @@ class df_config(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim",
                                        "ffn_hidden", "vocab", "n_experts", "top_k", "expert_hidden")] + [
         ("rope_theta", C.c_float), ("norm_eps", C.c_float), ("dtype", C.c_int),
-        ("max_batch", C.c_int), ("max_len", C.c_int), ("aux_top_k", C.c_int)]
+        ("max_batch", C.c_int), ("max_len", C.c_int), ("aux_top_k", C.c_int), ("page_len", C.c_int),
+        ("n_pages", C.c_int)]
 
 
 class df_weights(C.Structure):
@@ -46,7 +47,7 @@ _lib = None
 EXPORTS = ["df_workspace_bytes", "df_create", "df_prefill", "df_set_length", "df_decode_step",
            "df_decode_step_host", "df_set_mode", "df_debug_outputs", "df_sync", "df_length",
            "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc",
-           "df_generate"]
+           "df_generate", "df_set_batch", "df_prefill_seq", "df_release_seq", "df_seq_lengths", "df_seq_pages"]
 
 DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6, "layers": 7}
 
@@ -73,6 +74,16 @@ def lib():
     L.df_decode_step_noalloc.restype = i
     L.df_generate.argtypes = [vp, vp, i, C.c_ulonglong, vp, vp]
     L.df_generate.restype = i
+    L.df_set_batch.argtypes = [vp, i]
+    L.df_set_batch.restype = i
+    L.df_prefill_seq.argtypes = [vp, i, vp, i]
+    L.df_prefill_seq.restype = i
+    L.df_release_seq.argtypes = [vp, i]
+    L.df_release_seq.restype = i
+    L.df_seq_lengths.argtypes = [vp, P(C.c_int32)]
+    L.df_seq_lengths.restype = i
+    L.df_seq_pages.argtypes = [vp, i, P(C.c_int32), i]
+    L.df_seq_pages.restype = i
     L.df_decode_step_host.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step_host.restype = i
     L.df_set_mode.argtypes = [vp, i, i]
@@ -101,12 +112,12 @@ def check(ctx, status: int, what: str) -> None:
         raise DFError(status, f"{what}: {msg}")
 
 
-def make_config(cfg, max_batch: int, max_len: int) -> df_config:
+def make_config(cfg, max_batch: int, max_len: int, page_len: int = 0, n_pages: int = 0) -> df_config:
     return df_config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
                      cfg.ffn_hidden if not cfg.n_experts else 0, cfg.vocab, cfg.n_experts, cfg.top_k,
                      cfg.expert_hidden, float(cfg.rope_theta), float(cfg.norm_eps),
                      DF_BF16 if cfg.dtype == "bf16" else DF_F32, max_batch, max_len,
-                     getattr(cfg, "aux_top_k", 0) if cfg.n_experts else 0)
+                     getattr(cfg, "aux_top_k", 0) if cfg.n_experts else 0, page_len, n_pages)
 
 
 def df_workspace_bytes(c: df_config) -> tuple[int, int]:
@@ -169,6 +180,32 @@ def df_debug_outputs(ctx, logp1: int = 0, logp2: int = 0, topk: int = 0, router:
 
 def df_sync(ctx) -> None:
     check(ctx, lib().df_sync(ctx), "df_sync")
+
+
+def df_set_batch(ctx, B: int) -> None:
+    check(ctx, lib().df_set_batch(ctx, B), "df_set_batch")
+
+
+def df_prefill_seq(ctx, b: int, tokens_ptr: int, n: int) -> None:
+    check(ctx, lib().df_prefill_seq(ctx, b, C.c_void_p(tokens_ptr or None), n), "df_prefill_seq")
+
+
+def df_release_seq(ctx, b: int) -> None:
+    check(ctx, lib().df_release_seq(ctx, b), "df_release_seq")
+
+
+def df_seq_lengths(ctx, max_batch: int) -> list[int]:
+    out = (C.c_int32 * max_batch)()
+    check(ctx, lib().df_seq_lengths(ctx, out), "df_seq_lengths")
+    return list(out)
+
+
+def df_seq_pages(ctx, b: int, cap: int = 1 << 16) -> list[int]:
+    out = (C.c_int32 * cap)()
+    n = lib().df_seq_pages(ctx, b, out, cap)
+    if n < 0:
+        raise DFError(DF_ERR_ARG, "df_seq_pages: bad slot or contiguous cache")
+    return list(out[:min(n, cap)])
 
 
 def df_length(ctx) -> int:

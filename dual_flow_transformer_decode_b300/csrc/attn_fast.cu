@@ -92,7 +92,7 @@ __device__ __forceinline__ uint32_t sw_off(int pos, int dim) {
 
 __global__ void __launch_bounds__(160, 2)
     k_attn_tma(const __grid_constant__ CUtensorMap tkv, const float* __restrict__ qatt, Ctrl* __restrict__ ctrl,
-               __nv_bfloat16* __restrict__ out, int B, int Hkv, int G, int maxB, int layer, int flo, int fhi,
+               __nv_bfloat16* __restrict__ out, int B, int Hkv, int G, KvMap km, int layer, int flo, int fhi,
                int NS, int l2pf) {
   extern __shared__ uint8_t smem_raw[];
   cg::cluster_group cl = cg::this_cluster();
@@ -110,16 +110,18 @@ __global__ void __launch_bounds__(160, 2)
   const int R = (fhi - flo) * G;
   const int qdim = Hkv * G * HD;
 
-  // Positions 0..t: the cache below t was written by earlier steps, position
-  // t by the QKV kernel this kernel depends on.
-  const int t = ctrl->t;
+  // Positions 0..t of this sequence: the cache below t was written by earlier
+  // steps, position t by the QKV kernel this kernel depends on.
+  const int t = kv_seq_pos(km, ctrl, b);
   const int n = t + 1;
   int chunk = (n + splits - 1) / splits;
   chunk = (chunk + TP - 1) / TP * TP;
   const int s0 = s * chunk, s1 = min(n, s0 + chunk);
   const int ntiles = s1 > s0 ? (s1 - s0 + TP - 1) / TP : 0;
-  const int zK = ((layer * 2 + 0) * maxB + b) * Hkv + g;
-  const int zV = ((layer * 2 + 1) * maxB + b) * Hkv + g;
+  // tensor-map rows (z) of the K and V blocks of the page holding position
+  // p0, and the position's offset in it (y); a 64-position tile never spans
+  // two pages (pages hold a multiple of 64 positions)
+  auto tile_z = [&](int p0, int kvsel) { return ((layer * 2 + kvsel) * km.NP + kv_page(km, b, p0)) * Hkv + g; };
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -140,21 +142,23 @@ __global__ void __launch_bounds__(160, 2)
     for (; issued < pre; ++issued) {
       const int p0 = s0 + issued * TP;
       if (p0 + TP > t) break;
+      const int zK = tile_z(p0, 0), zV = tile_z(p0, 1), y = kv_off(km, p0);
       uint8_t* dst = ring + issued * STAGE;
       ptx::mbar_arrive_expect_tx(&full[issued], STAGE);
-      ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[issued], 0, p0, zK);
-      ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[issued], 64, p0, zK);
-      ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[issued], 0, p0, zV);
-      ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[issued], 64, p0, zV);
+      ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[issued], 0, y, zK);
+      ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[issued], 64, y, zK);
+      ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[issued], 0, y, zV);
+      ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[issued], 64, y, zV);
     }
     if (l2pf)
       for (int i = issued; i < ntiles; ++i) {
         const int p0 = s0 + i * TP;
         if (p0 + TP > t) break;
-        ptx::tma_prefetch_3d(&tkv, 0, p0, zK);
-        ptx::tma_prefetch_3d(&tkv, 64, p0, zK);
-        ptx::tma_prefetch_3d(&tkv, 0, p0, zV);
-        ptx::tma_prefetch_3d(&tkv, 64, p0, zV);
+        const int zK = tile_z(p0, 0), zV = tile_z(p0, 1), y = kv_off(km, p0);
+        ptx::tma_prefetch_3d(&tkv, 0, y, zK);
+        ptx::tma_prefetch_3d(&tkv, 64, y, zK);
+        ptx::tma_prefetch_3d(&tkv, 0, y, zV);
+        ptx::tma_prefetch_3d(&tkv, 64, y, zV);
       }
   }
   ptx::grid_dep_wait();
@@ -198,12 +202,13 @@ __global__ void __launch_bounds__(160, 2)
         }
         if (*abort_flag) break;
         const int p0 = s0 + i * TP;
+        const int zK = tile_z(p0, 0), zV = tile_z(p0, 1), y = kv_off(km, p0);
         uint8_t* dst = ring + st * STAGE;
         ptx::mbar_arrive_expect_tx(&full[st], STAGE);
-        ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[st], 0, p0, zK);
-        ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[st], 64, p0, zK);
-        ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[st], 0, p0, zV);
-        ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[st], 64, p0, zV);
+        ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[st], 0, y, zK);
+        ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[st], 64, y, zK);
+        ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[st], 0, y, zV);
+        ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[st], 64, y, zV);
         issued = i + 1;
       }
       if (*abort_flag) {
@@ -450,8 +455,9 @@ bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err) {
       q != cudaDriverEntryPointSuccess || !fn)
     return true;
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)D.max_len, (cuuint64_t)D.L * 2 * D.maxB * D.Hkv};
-  cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)D.max_len * HD * 2};
+  // (head_dim, positions of a page, L * 2 * pages * KV heads)
+  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)D.PG, (cuuint64_t)D.L * 2 * D.NP * D.Hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)D.PG * HD * 2};
   cuuint32_t box[3] = {64, TP, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(&P.kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, kv, dims, strides, box, estr,
@@ -496,7 +502,7 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   lc.attrs = at;
   lc.numAttrs = 2;
   cudaLaunchKernelEx(&lc, k_attn_tma, P.kv, (const float*)Bf.qatt, Bf.ctrl, (__nv_bfloat16*)Bf.o, R.B, D.Hkv, D.G,
-                     D.maxB, layer, flo, fhi, ns, l2pf);
+                     Bf.kvm, layer, flo, fhi, ns, l2pf);
 }
 
 }  // namespace df

@@ -11,7 +11,7 @@ namespace df {
 
 struct AttnPlan {
   bool enabled = false;
-  CUtensorMap kv;   // 3-D view: (head_dim, max_len, L*2*maxB*Hkv)
+  CUtensorMap kv;   // 3-D view: (head_dim, positions of a page, L*2*pages*Hkv)
 };
 
 bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err);

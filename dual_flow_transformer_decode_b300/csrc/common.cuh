@@ -17,12 +17,40 @@ struct Ctrl {
   int err_info;   // kernel-specific detail for the first error
   int mk_abort;   // set by a persistent-kernel CTA that gave up; the others stop waiting
   unsigned long long seed;  // key of the sampling noise (generation)
-  int pad[58];
+  int gen_row;    // generation: history row of the current step (reset with the seed)
+  int pad[57];
 };
 static_assert(sizeof(Ctrl) == 256, "control block layout");
 
 __device__ __forceinline__ void latch_error(Ctrl* c, int code, int info) {
   if (atomicCAS(&c->err, 0, code) == 0) c->err_info = info;
+}
+
+// KV-cache addressing.  The cache is [L][2][NP][Hkv][PG][hd]: per layer a K
+// block then a V block, each made of NP pages of PG positions per KV head.
+// Paged mode: position p of sequence b lives in page
+// table[b*MPS + (p >> pg_shift)] at offset p & (PG - 1), and each sequence
+// has its own position pos[b].  Contiguous mode (table == nullptr): one page
+// of max_len positions per sequence (page b, offset p) and every sequence at
+// position ctrl->t.
+struct KvMap {
+  const int* table;  // [maxB][MPS] physical page of each logical page, or nullptr
+  const int* pos;    // [maxB] current position of each sequence (paged mode)
+  const int* active; // [maxB] 1 for sequences that advance (paged mode)
+  int NP, PG, MPS, pg_shift;
+};
+
+__device__ __forceinline__ int kv_seq_pos(const KvMap& m, const Ctrl* c, int b) {
+  return m.table ? m.pos[b] : c->t;
+}
+__device__ __forceinline__ int kv_page(const KvMap& m, int b, int p) {
+  return m.table ? m.table[b * m.MPS + (p >> m.pg_shift)] : b;
+}
+__device__ __forceinline__ int kv_off(const KvMap& m, int p) { return m.table ? (p & (m.PG - 1)) : p; }
+// Element index of (layer, kv = 0 for K / 1 for V, page, KV head g, offset).
+__device__ __forceinline__ size_t kv_index(const KvMap& m, int Hkv, int hd, int layer, int kv, int page, int g,
+                                           int off) {
+  return ((((size_t)(layer * 2 + kv) * m.NP + page) * Hkv + g) * m.PG + off) * hd;
 }
 
 // Philox4x64 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random

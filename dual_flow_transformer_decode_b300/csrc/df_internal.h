@@ -42,11 +42,21 @@ struct Dims {
   int qdim, kvdim, qkvn, G, Fm;   // Fm = MLP hidden of one expert or of the dense MLP
   int esz;         // element size of dtype
   int sms;         // streaming multiprocessors of the device
+  // KV-cache pages (see KvMap): contiguous mode NP = maxB, PG = max_len,
+  // MPS = 1; paged mode NP = pool pages + 1 (the last is a sink written by
+  // free slots), PG a power of two >= 64, MPS = ceil(max_len / PG)
+  int paged, NP, PG, MPS, pg_shift;
+  size_t kv_layer_elems() const { return (size_t)2 * NP * Hkv * PG * hd; }  // one layer's K and V blocks
+  size_t kv_half_elems() const { return (size_t)NP * Hkv * PG * hd; }       // the K (or V) block of a layer
 };
 
 // Device buffers carved out of the caller's workspace.
 struct Buffers {
   Ctrl* ctrl;
+  KvMap kvm;        // cache addressing (page table, positions, active flags in paged mode)
+  int* kv_table;    // paged mode: [maxB][MPS] page table
+  int* kv_pos;      // paged mode: [maxB] positions
+  int* kv_active;   // paged mode: [maxB] active flags
   int* tokbuf;      // [maxB]   tokens of a host-buffer step
   float* h;         // [2maxB][d] fp32 residual rows (0..B-1 primary, B..2B-1 auxiliary)
   void* u;          // [Mpad][d]  normed rows (GEMM input, dtype)
@@ -114,7 +124,17 @@ struct Couple {
 // ------------------------------------------------------------ basic kernels
 void kernels_init();   // one-time function attributes (dynamic shared memory limits)
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s);
-void launch_advance_pos(Ctrl* c, cudaStream_t s);
+// End of a pass: step counter + 1; paged mode: positions of the active
+// sequences in [lo, hi) + 1.
+void launch_advance_pos(const Buffers& Bf, int lo, int hi, cudaStream_t s);
+// Up to kIntEdits writes dst[idx[i]] = val[i], in order, on the stream.
+constexpr int kIntEdits = 48;
+struct IntEdits {
+  int n;
+  int idx[kIntEdits];
+  int val[kIntEdits];
+};
+void launch_int_edits(int* dst, const IntEdits& e, cudaStream_t s);
 void launch_set_seed(Ctrl* c, unsigned long long seed, cudaStream_t s);
 void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void* emb2,
                   const int32_t* tokens, int tok_stride, int use_pos, const Rows& R, cudaStream_t s);

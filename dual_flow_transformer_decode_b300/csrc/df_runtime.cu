@@ -15,6 +15,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -91,6 +92,12 @@ struct df_ctx {
   df::MkPlan mk;
   df::BpPlan bp;
   std::string err;
+  // paged mode: the page pool as the host tracks it (the device table and
+  // positions mirror it; every change is enqueued before the work that
+  // depends on it)
+  std::vector<int> free_pages;              // stack of free physical pages
+  std::vector<std::vector<int>> seq_pages;  // per slot: physical page of each logical page
+  std::vector<int> seq_len;                 // per slot: length, -1 for a free slot
 };
 
 namespace {
@@ -130,6 +137,16 @@ bool valid_config(const df_config* c, std::string* why) {
   }
   if (c->n_experts > 4096) return bad("n_experts above 4096");
   if (!(c->norm_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("norm_eps and rope_theta must be positive");
+  if (c->page_len) {
+    if (c->page_len < 64 || c->page_len > (1 << 20) || (c->page_len & (c->page_len - 1)))
+      return bad("page_len must be 0 or a power of two in [64, 2^20]");
+    if (c->n_pages <= 0) return bad("n_pages must be positive in paged mode");
+    // tensor-map rows of the cache: n_layers * 2 * (n_pages + 1) * n_kv_heads
+    if ((double)c->n_layers * 2 * ((double)c->n_pages + 1) * c->n_kv_heads >= 2147483647.0)
+      return bad("page pool too large");
+  } else if (c->n_pages) {
+    return bad("n_pages needs page_len");
+  }
   return true;
 }
 
@@ -157,6 +174,22 @@ Dims make_dims(const df_config* c) {
   D.G = D.Hq / D.Hkv;
   D.Fm = D.E ? D.Fe : D.F;
   D.esz = D.bf16 ? 2 : 4;
+  if (c->page_len) {
+    D.paged = 1;
+    D.PG = c->page_len;
+    D.NP = c->n_pages + 1;  // the last page is the sink of free slots
+    // one more column than the positions need: a full sequence (position
+    // max_len) still maps to an entry, the sink
+    D.MPS = D.max_len / D.PG + 1;
+    D.pg_shift = 0;
+    while ((1 << D.pg_shift) < D.PG) ++D.pg_shift;
+  } else {
+    D.paged = 0;
+    D.PG = D.max_len;
+    D.NP = D.maxB;
+    D.MPS = 1;
+    D.pg_shift = 0;
+  }
   // the split plan and workspace size depend on the SM count of the current device
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -177,6 +210,10 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   size_t esz = D.esz;
   Buffers b{};
   b.ctrl = (df::Ctrl*)take(sizeof(df::Ctrl));
+  b.kv_table = (int*)take(D.paged ? (size_t)D.maxB * D.MPS * 4 : 0);
+  b.kv_pos = (int*)take((size_t)D.maxB * 4);
+  b.kv_active = (int*)take((size_t)D.maxB * 4);
+  b.kvm = df::KvMap{D.paged ? b.kv_table : nullptr, b.kv_pos, b.kv_active, D.NP, D.PG, D.MPS, D.pg_shift};
   b.tokbuf = (int*)take(D.maxB * 4);
   b.h = (float*)take(M2 * D.d * 4);
   b.u = take(Mpad * D.d * esz);
@@ -221,7 +258,7 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.out_alpha = (float*)take(D.maxB * 4);
   b.gen_tok = (int*)take(D.maxB * 4);
   b.gen_hist = (int*)take((size_t)D.max_len * D.maxB * 4);
-  b.rope = (float*)take((size_t)D.max_len * D.hd * 4);
+  b.rope = (float*)take((size_t)(D.max_len + 1) * D.hd * 4);
   b.tickets_cap = df::tc_tickets_needed(D);
   b.tickets = (int*)take(b.tickets_cap * 4);
   b.attn_tickets = (int*)take((size_t)D.maxB * D.Hkv * 4);
@@ -235,9 +272,7 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   return cur;
 }
 
-size_t kv_size(const Dims& D) {
-  return (size_t)D.L * 2 * D.maxB * D.Hkv * D.max_len * D.hd * D.esz;
-}
+size_t kv_size(const Dims& D) { return (size_t)D.L * D.kv_layer_elems() * D.esz; }
 
 // ---------------------------------------------------------------- step sequencing
 
@@ -394,14 +429,98 @@ void enqueue_decode(df_ctx* X, const int32_t* tokens, const StepOut& o) {
   }
   df::launch_mix(D, X->Bf, B, X->aux_on, o.logp_mix, o.argmax, o.alpha, X->dbg_logp1, X->aux_on ? X->dbg_logp2 : nullptr,
                  o.sample_tok, o.sample_hist, s);
-  df::launch_advance_pos(X->Bf.ctrl, s);
+  df::launch_advance_pos(X->Bf, 0, B, s);
 }
 
-void enqueue_prefill_pos(df_ctx* X, const int32_t* tokens, int n) {
+// One token-serial prefill position over all B primary rows.  Row b embeds
+// tokens[b*stride + step] (step = the pass counter, reset before the first
+// position); positions advance for the sequences [adv_lo, adv_hi) only.
+void enqueue_prefill_pos(df_ctx* X, const int32_t* tokens, int stride, int adv_lo, int adv_hi) {
   Rows R{X->B, 0, X->B};
-  df::launch_embed(X->D, X->Bf, X->emb1, X->emb2, tokens, n, 1, R, X->stream);
+  df::launch_embed(X->D, X->Bf, X->emb1, X->emb2, tokens, stride, 1, R, X->stream);
   enqueue_pass(X, R, 0, 0, false);
-  df::launch_advance_pos(X->Bf.ctrl, X->stream);
+  df::launch_advance_pos(X->Bf, adv_lo, adv_hi, X->stream);
+}
+
+// ------------------------------------------------------------------ paged mode
+
+// Writes into one device int array (page table, positions or active flags),
+// queued and flushed as small kernels on the context's stream.
+struct EditQueue {
+  df_ctx* X;
+  int* dst;
+  df::IntEdits e{};
+  void add(int idx, int val) {
+    if (e.n == df::kIntEdits) flush();
+    e.idx[e.n] = idx;
+    e.val[e.n] = val;
+    ++e.n;
+  }
+  void flush() {
+    df::launch_int_edits(dst, e, X->stream);
+    e.n = 0;
+  }
+};
+
+int pages_for(const Dims& D, int n) { return (n + D.PG - 1) / D.PG; }
+
+// Returns slot b's pages to the pool and points its table row at the sink.
+void release_slot(df_ctx* X, int b, EditQueue& tq) {
+  auto& pg = X->seq_pages[b];
+  for (int i = (int)pg.size() - 1; i >= 0; --i) {
+    X->free_pages.push_back(pg[i]);
+    tq.add(b * X->D.MPS + i, X->D.NP - 1);
+  }
+  pg.clear();
+  X->seq_len[b] = -1;
+}
+
+// Maps positions [0, n) of slot b, taking pages from the pool; false (and
+// nothing taken) when the pool is short.
+bool grow_slot(df_ctx* X, int b, int n, EditQueue& tq) {
+  auto& pg = X->seq_pages[b];
+  const int need = pages_for(X->D, n) - (int)pg.size();
+  if (need > (int)X->free_pages.size()) return false;
+  for (int i = 0; i < need; ++i) {
+    const int p = X->free_pages.back();
+    X->free_pages.pop_back();
+    tq.add(b * X->D.MPS + (int)pg.size(), p);
+    pg.push_back(p);
+  }
+  return true;
+}
+
+// Before n decode steps: capacity checks (nothing enqueued on failure), then
+// the pages the steps will write are mapped.  Contiguous mode: the common
+// position must leave room for n steps.
+df_status prepare_steps(df_ctx* X, int n, const char* who) {
+  const Dims& D = X->D;
+  if (!D.paged) {
+    if (n > X->cfg.max_len - X->t) return fail(X, DF_ERR_CAPACITY, std::string(who) + ": cache full (t + steps > max_len)");
+    return DF_OK;
+  }
+  int need = 0;
+  for (int b = 0; b < X->B; ++b) {
+    const int len = X->seq_len[b];
+    if (len < 0) continue;
+    if (n > X->cfg.max_len - len)
+      return fail(X, DF_ERR_CAPACITY, std::string(who) + ": sequence " + std::to_string(b) + " would pass max_len");
+    need += std::max(0, pages_for(D, len + n) - (int)X->seq_pages[b].size());
+  }
+  if (need > (int)X->free_pages.size())
+    return fail(X, DF_ERR_CAPACITY, std::string(who) + ": page pool exhausted");
+  EditQueue tq{X, X->Bf.kv_table};
+  for (int b = 0; b < X->B; ++b)
+    if (X->seq_len[b] >= 0) grow_slot(X, b, X->seq_len[b] + n, tq);
+  tq.flush();
+  return DF_OK;
+}
+
+void finish_steps(df_ctx* X, int n) {
+  X->t += n;
+  if (X->D.paged)
+    for (int b = 0; b < X->B; ++b)
+      if (X->seq_len[b] >= 0) X->seq_len[b] += n;
 }
 
 int count_kernel_nodes(cudaGraph_t g) {
@@ -457,11 +576,43 @@ df_status run_captured(df_ctx* X, GraphSlot& slot, const GraphKey& key, F&& enqu
   return DF_OK;
 }
 
+// Prefill of n positions: all B sequences (nseq = B, slot0 = 0) or one slot
+// (nseq = 1).  Positions must start at 0 (set by the caller).
+df_status prefill_rows(df_ctx* X, const int32_t* tokens, int nseq, int n, int slot0, int B) {
+  if (X->bp.enabled && X->tc.enabled && X->at.enabled && !X->force_generic) {
+    // batched: every layer once per chunk of positions (kernels enqueued directly)
+    df::bp_prefill(X->bp, X->tc, X->at, X->D, X->Bf, X->kv, X->emb1, X->attn_norm.data(), X->mlp_norm.data(),
+                   tokens, nseq, n, slot0, X->stream);
+    df::launch_set_pos(X->Bf.ctrl, n, X->stream);
+    if (X->D.paged) {
+      EditQueue pq{X, X->Bf.kv_pos};
+      for (int b = slot0; b < slot0 + nseq; ++b) pq.add(b, n);
+      pq.flush();
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(X, e, "batched prefill launch");
+    X->last_kernels = -1;
+    return DF_OK;
+  }
+  // token-serial: one pass over all B primary rows per position; for one
+  // slot the other rows compute at their own positions, where any value
+  // written is rewritten by their next decode step before it is read
+  GraphKey key{};
+  key.p[0] = tokens;
+  key.i[0] = n;
+  key.i[1] = B;
+  key.i[2] = X->force_generic;
+  key.i[3] = nseq;
+  key.i[4] = slot0;
+  const int stride = nseq == 1 && B > 1 ? 0 : n;
+  return run_captured(X, X->pre, key, [&] { enqueue_prefill_pos(X, tokens, stride, slot0, slot0 + nseq); }, n);
+}
+
 void setup_rope(df_ctx* X, std::vector<float>& host) {
   const Dims& D = X->D;
   int half = D.hd / 2;
-  host.assign((size_t)D.max_len * D.hd, 0.f);
-  for (int t = 0; t < D.max_len; ++t)
+  host.assign((size_t)(D.max_len + 1) * D.hd, 0.f);
+  for (int t = 0; t <= D.max_len; ++t)
     for (int i = 0; i < half; ++i) {
       double ang = (double)t * std::pow((double)D.theta, -2.0 * i / D.hd);
       host[(size_t)t * D.hd + 2 * i] = (float)std::cos(ang);
@@ -541,9 +692,19 @@ df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, voi
   df::kernels_init();
   std::vector<float> rope;
   setup_rope(X, rope);
+  X->seq_len.assign(X->D.maxB, -1);
+  X->seq_pages.assign(X->D.maxB, {});
+  std::vector<int> table;
+  if (X->D.paged) {
+    for (int p = X->D.NP - 2; p >= 0; --p) X->free_pages.push_back(p);  // page 0 is taken first
+    table.assign((size_t)X->D.maxB * X->D.MPS, X->D.NP - 1);             // every entry at the sink
+  }
   cudaError_t e = cudaMemsetAsync(X->ws, 0, ws_bytes, X->stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(X->Bf.rope, rope.data(), rope.size() * sizeof(float), cudaMemcpyHostToDevice, X->stream);
+  if (e == cudaSuccess && !table.empty())
+    e = cudaMemcpyAsync(X->Bf.kv_table, table.data(), table.size() * sizeof(int), cudaMemcpyHostToDevice,
+                        X->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(X->stream);
   if (e != cudaSuccess) {
     fprintf(stderr, "df_create: %s\n", cudaGetErrorString(e));
@@ -568,6 +729,18 @@ df_status df_create(const df_config* cfg, const df_weights* w, void* kv_buf, voi
 }
 
 static df_status set_batch(df_ctx* X, int B) {
+  if (X->D.paged && B < X->B) {
+    EditQueue tq{X, X->Bf.kv_table}, aq{X, X->Bf.kv_active}, pq{X, X->Bf.kv_pos};
+    for (int b = B; b < X->B; ++b)
+      if (X->seq_len[b] >= 0) {
+        release_slot(X, b, tq);
+        aq.add(b, 0);
+        pq.add(b, 0);
+      }
+    tq.flush();
+    aq.flush();
+    pq.flush();
+  }
   if (B != X->B) {
     X->dec.reset();
     X->pre.reset();
@@ -587,41 +760,60 @@ df_status df_prefill(df_ctx* X, const int32_t* tokens, int B, int n) {
   if (B <= 0 || n < 0 || (n > 0 && !tokens)) return fail(X, DF_ERR_ARG, "df_prefill: bad arguments");
   if (B > X->cfg.max_batch) return fail(X, DF_ERR_CAPACITY, "df_prefill: B > max_batch");
   if (n > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_prefill: n > max_len");
+  if (X->D.paged && (size_t)B * pages_for(X->D, n) > (size_t)(X->D.NP - 1))
+    return fail(X, DF_ERR_CAPACITY, "df_prefill: page pool too small for B sequences of n positions");
   df_status st = set_batch(X, B);
   if (st != DF_OK) return st;
+  if (X->D.paged) {
+    // every slot of the batch starts over: n positions, all active
+    EditQueue tq{X, X->Bf.kv_table}, aq{X, X->Bf.kv_active}, pq{X, X->Bf.kv_pos};
+    for (int b = 0; b < B; ++b)
+      if (X->seq_len[b] >= 0) release_slot(X, b, tq);
+    for (int b = 0; b < B; ++b) {
+      grow_slot(X, b, n, tq);
+      X->seq_len[b] = n;
+      aq.add(b, 1);
+      pq.add(b, 0);
+    }
+    tq.flush();
+    aq.flush();
+    pq.flush();
+  }
   df::launch_set_pos(X->Bf.ctrl, 0, X->stream);
   X->t = 0;
   X->ready = true;
   if (n == 0) return DF_OK;
-  if (X->bp.enabled && X->tc.enabled && X->at.enabled && !X->force_generic) {
-    // batched: every layer once per chunk of positions (kernels enqueued directly)
-    df::bp_prefill(X->bp, X->tc, X->at, X->D, X->Bf, X->kv, X->emb1, X->attn_norm.data(), X->mlp_norm.data(),
-                   tokens, B, n, X->stream);
-    df::launch_set_pos(X->Bf.ctrl, n, X->stream);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(X, e, "batched prefill launch");
-    X->last_kernels = -1;
-    X->t = n;
-    return DF_OK;
-  }
-  GraphKey key{};
-  key.p[0] = tokens;
-  key.i[0] = n;
-  key.i[1] = B;
-  key.i[2] = X->force_generic;
-  st = run_captured(X, X->pre, key, [&] { enqueue_prefill_pos(X, tokens, n); }, n);
+  st = prefill_rows(X, tokens, B, n, 0, B);
   if (st != DF_OK) return st;
   X->t = n;
   return DF_OK;
 }
+
+
 
 df_status df_set_length(df_ctx* X, int B, int t) {
   if (!X) return DF_ERR_ARG;
   if (B <= 0 || t < 0) return fail(X, DF_ERR_ARG, "df_set_length: bad arguments");
   if (B > X->cfg.max_batch) return fail(X, DF_ERR_CAPACITY, "df_set_length: B > max_batch");
   if (t > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_set_length: t > max_len");
+  if (X->D.paged && (size_t)B * pages_for(X->D, t) > (size_t)(X->D.NP - 1))
+    return fail(X, DF_ERR_CAPACITY, "df_set_length: page pool too small");
   df_status st = set_batch(X, B);
   if (st != DF_OK) return st;
+  if (X->D.paged) {
+    EditQueue tq{X, X->Bf.kv_table}, aq{X, X->Bf.kv_active}, pq{X, X->Bf.kv_pos};
+    for (int b = 0; b < B; ++b)
+      if (X->seq_len[b] >= 0) release_slot(X, b, tq);
+    for (int b = 0; b < B; ++b) {
+      grow_slot(X, b, t, tq);
+      X->seq_len[b] = t;
+      aq.add(b, 1);
+      pq.add(b, t);
+    }
+    tq.flush();
+    aq.flush();
+    pq.flush();
+  }
   df::launch_set_pos(X->Bf.ctrl, t, X->stream);
   X->t = t;
   X->ready = true;
@@ -633,7 +825,8 @@ df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int3
   if (!X) return DF_ERR_ARG;
   if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step: null tokens");
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step before df_prefill");
-  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step: cache full (t >= max_len)");
+  df_status pst = prepare_steps(X, 1, "df_decode_step");
+  if (pst != DF_OK) return pst;
   GraphKey key{};
   key.p[0] = tokens;
   key.p[1] = logp_mix;
@@ -650,7 +843,7 @@ df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int3
   StepOut o{logp_mix, argmax, alpha};
   df_status st = run_captured(X, X->dec, key, [&] { enqueue_decode(X, tokens, o); }, 1);
   if (st != DF_OK) return st;
-  X->t += 1;
+  finish_steps(X, 1);
   return DF_OK;
 }
 
@@ -660,9 +853,11 @@ df_status df_generate(df_ctx* X, const int32_t* tokens, int n_steps, unsigned lo
   if (n_steps < 0) return fail(X, DF_ERR_ARG, "df_generate: n_steps < 0");
   if (n_steps > 0 && (!tokens || !out_tokens)) return fail(X, DF_ERR_ARG, "df_generate: null tokens or out_tokens");
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_generate before df_prefill");
-  if (n_steps > X->cfg.max_len - X->t) return fail(X, DF_ERR_CAPACITY, "df_generate: t + n_steps > max_len");
+  if (n_steps > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_generate: n_steps > max_len");
   if (n_steps == 0) return DF_OK;
-  const int B = X->B, t0 = X->t;
+  df_status pst = prepare_steps(X, n_steps, "df_generate");
+  if (pst != DF_OK) return pst;
+  const int B = X->B;
   cudaError_t e = cudaSuccess;
   if (tokens != X->Bf.gen_tok)
     e = cudaMemcpyAsync(X->Bf.gen_tok, tokens, (size_t)B * 4, cudaMemcpyDeviceToDevice, X->stream);
@@ -682,9 +877,9 @@ df_status df_generate(df_ctx* X, const int32_t* tokens, int n_steps, unsigned lo
   StepOut o{logp_mix, nullptr, nullptr, X->Bf.gen_tok, X->Bf.gen_hist};
   df_status st = run_captured(X, X->gen, key, [&] { enqueue_decode(X, X->Bf.gen_tok, o); }, n_steps);
   if (st != DF_OK) return st;
-  X->t += n_steps;
-  e = cudaMemcpy2DAsync(out_tokens, (size_t)B * 4, X->Bf.gen_hist + (size_t)t0 * X->D.maxB, (size_t)X->D.maxB * 4,
-                        (size_t)B * 4, n_steps, cudaMemcpyDeviceToDevice, X->stream);
+  finish_steps(X, n_steps);
+  e = cudaMemcpy2DAsync(out_tokens, (size_t)B * 4, X->Bf.gen_hist, (size_t)X->D.maxB * 4, (size_t)B * 4, n_steps,
+                        cudaMemcpyDeviceToDevice, X->stream);
   if (e != cudaSuccess) return cuda_fail(X, e, "df_generate: output copy");
   return DF_OK;
 }
@@ -715,7 +910,8 @@ df_status df_decode_step_host(df_ctx* X, const int32_t* tokens, float* logp_mix,
   if (!X) return DF_ERR_ARG;
   if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_host: null tokens");
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_host before df_prefill");
-  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step_host: cache full");
+  df_status pst = prepare_steps(X, 1, "df_decode_step_host");  // capacity before any copy
+  if (pst != DF_OK) return pst;
   int B = X->B, V = X->D.V;
   cudaError_t e = cudaMemcpyAsync(X->Bf.tokbuf, tokens, B * sizeof(int32_t), cudaMemcpyHostToDevice, X->stream);
   if (e != cudaSuccess) return cuda_fail(X, e, "token copy");
@@ -785,7 +981,85 @@ df_status df_time_op(df_ctx* X, int op, int iters, float* avg_ms) {
   return DF_OK;
 }
 
-int df_length(const df_ctx* X) { return X ? X->t : -1; }
+int df_length(const df_ctx* X) {
+  if (!X) return -1;
+  if (!X->D.paged) return X->t;
+  int m = 0;
+  for (int b = 0; b < X->B; ++b) m = std::max(m, X->seq_len[b]);
+  return m;
+}
+
+df_status df_set_batch(df_ctx* X, int B) {
+  if (!X) return DF_ERR_ARG;
+  if (!X->D.paged) return fail(X, DF_ERR_UNSUPPORTED, "df_set_batch: needs a paged cache (page_len > 0)");
+  if (B <= 0 || B > X->cfg.max_batch) return fail(X, DF_ERR_ARG, "df_set_batch: B outside [1, max_batch]");
+  df_status st = set_batch(X, B);
+  if (st != DF_OK) return st;
+  X->ready = true;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DF_OK : cuda_fail(X, e, "df_set_batch");
+}
+
+df_status df_prefill_seq(df_ctx* X, int b, const int32_t* tokens, int n) {
+  if (!X) return DF_ERR_ARG;
+  if (!X->D.paged) return fail(X, DF_ERR_UNSUPPORTED, "df_prefill_seq: needs a paged cache (page_len > 0)");
+  if (!X->ready || X->B <= 0) return fail(X, DF_ERR_STATE, "df_prefill_seq before df_set_batch or df_prefill");
+  if (b < 0 || b >= X->B || n < 0 || (n > 0 && !tokens)) return fail(X, DF_ERR_ARG, "df_prefill_seq: bad arguments");
+  if (n > X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_prefill_seq: n > max_len");
+  EditQueue tq{X, X->Bf.kv_table}, aq{X, X->Bf.kv_active}, pq{X, X->Bf.kv_pos};
+  const int had = (int)X->seq_pages[b].size();
+  if (pages_for(X->D, n) > (int)X->free_pages.size() + had)
+    return fail(X, DF_ERR_CAPACITY, "df_prefill_seq: page pool exhausted");
+  if (X->seq_len[b] >= 0) release_slot(X, b, tq);
+  grow_slot(X, b, n, tq);
+  X->seq_len[b] = n;
+  aq.add(b, 1);
+  pq.add(b, 0);
+  tq.flush();
+  aq.flush();
+  pq.flush();
+  if (n > 0) {
+    df::launch_set_pos(X->Bf.ctrl, 0, X->stream);
+    df_status st = prefill_rows(X, tokens, 1, n, b, X->B);
+    if (st != DF_OK) return st;
+  }
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DF_OK : cuda_fail(X, e, "df_prefill_seq");
+}
+
+df_status df_release_seq(df_ctx* X, int b) {
+  if (!X) return DF_ERR_ARG;
+  if (!X->D.paged) return fail(X, DF_ERR_UNSUPPORTED, "df_release_seq: needs a paged cache (page_len > 0)");
+  if (b < 0 || b >= X->cfg.max_batch) return fail(X, DF_ERR_ARG, "df_release_seq: bad slot");
+  if (X->seq_len[b] < 0) return DF_OK;
+  EditQueue tq{X, X->Bf.kv_table}, aq{X, X->Bf.kv_active}, pq{X, X->Bf.kv_pos};
+  release_slot(X, b, tq);
+  aq.add(b, 0);
+  pq.add(b, 0);
+  tq.flush();
+  aq.flush();
+  pq.flush();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DF_OK : cuda_fail(X, e, "df_release_seq");
+}
+
+df_status df_seq_lengths(const df_ctx* X, int32_t* lengths) {
+  if (!X || !lengths) return DF_ERR_ARG;
+  for (int b = 0; b < X->cfg.max_batch; ++b) {
+    if (X->D.paged)
+      lengths[b] = b < X->B ? X->seq_len[b] : -1;
+    else
+      lengths[b] = (X->ready && b < X->B) ? X->t : -1;
+  }
+  return DF_OK;
+}
+
+int df_seq_pages(const df_ctx* X, int b, int32_t* pages, int cap) {
+  if (!X || !X->D.paged || b < 0 || b >= X->cfg.max_batch) return -1;
+  const auto& pg = X->seq_pages[b];
+  for (int i = 0; i < (int)pg.size() && i < cap; ++i) pages[i] = pg[i];
+  return (int)pg.size();
+}
 
 int df_step_kernels(const df_ctx* X) { return X ? X->last_kernels : -1; }
 
@@ -853,7 +1127,6 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
   if (!X) return DF_ERR_ARG;
   if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_noalloc: null tokens");
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_noalloc before df_prefill");
-  if (X->t >= X->cfg.max_len) return fail(X, DF_ERR_CAPACITY, "df_decode_step_noalloc: cache full (t >= max_len)");
   const size_t parts = (size_t)X->B * X->D.Hkv * X->splits * 2 * X->D.G;
   const size_t need = parts * (X->D.hd + 2);
   if (need > kStaticScratchFloats) {
@@ -866,6 +1139,8 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
   float* scratch = nullptr;
   cudaError_t e = static_scratch(&scratch);
   if (e != cudaSuccess) return cuda_fail(X, e, "cudaGetSymbolAddress");
+  df_status pst = prepare_steps(X, 1, "df_decode_step_noalloc");
+  if (pst != DF_OK) return pst;
   GraphKey key{};
   key.p[0] = tokens;
   key.p[1] = logp_mix;
@@ -893,6 +1168,6 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
   X->Bf = saved;
   X->mk.apart = saved_apart;
   if (st != DF_OK) return st;
-  X->t += 1;
+  finish_steps(X, 1);
   return DF_OK;
 }

@@ -27,22 +27,39 @@ __global__ void k_set_pos(Ctrl* c, int t) {
   ptx::grid_dep_launch();
   c->t = t;
 }
-__global__ void k_advance_pos(Ctrl* c) {
+// End of a pass: the step counter, the generation history row and, in paged
+// mode, the positions of the active sequences in [lo, hi) advance by one.
+__global__ void k_advance_pos(Ctrl* c, int* pos, const int* active, int lo, int hi) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  c->t += 1;
+  if (threadIdx.x == 0) {
+    c->t += 1;
+    c->gen_row += 1;
+  }
+  if (pos)
+    for (int b = lo + (int)threadIdx.x; b < hi; b += blockDim.x)
+      if (active[b]) pos[b] += 1;
 }
 __global__ void k_set_seed(Ctrl* c, unsigned long long seed) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   c->seed = seed;
+  c->gen_row = 0;
+}
+// Paged mode: writes up to kIntEdits (index, value) pairs into an int array
+// (page-table entries, positions, active flags), in order.
+__global__ void k_int_edits(int* dst, IntEdits e) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (threadIdx.x == 0)
+    for (int i = 0; i < e.n; ++i) dst[e.idx[i]] = e.val[i];
 }
 
 template <typename T>
-__global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
+__global__ void k_attn_generic(const T* __restrict__ kv, int layer, KvMap km, const float* __restrict__ qatt,
                                const Ctrl* __restrict__ ctrl, float* __restrict__ part_o,
-                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
-                               int splits, int flo, int fhi);
+                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int splits, int flo,
+                               int fhi);
 
 bool pdl_enabled() {
   static int v = -1;
@@ -68,7 +85,13 @@ void kernels_init() {
 }
 
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { launch_pdl(k_set_pos, dim3(1), dim3(1), 0, s, c, t); }
-void launch_advance_pos(Ctrl* c, cudaStream_t s) { launch_pdl(k_advance_pos, dim3(1), dim3(1), 0, s, c); }
+void launch_advance_pos(const Buffers& Bf, int lo, int hi, cudaStream_t s) {
+  launch_pdl(k_advance_pos, dim3(1), dim3(128), 0, s, Bf.ctrl, Bf.kvm.table ? Bf.kv_pos : (int*)nullptr,
+             (const int*)Bf.kv_active, lo, hi);
+}
+void launch_int_edits(int* dst, const IntEdits& e, cudaStream_t s) {
+  if (e.n > 0) launch_pdl(k_int_edits, dim3(1), dim3(32), 0, s, dst, e);
+}
 void launch_set_seed(Ctrl* c, unsigned long long seed, cudaStream_t s) {
   launch_pdl(k_set_seed, dim3(1), dim3(1), 0, s, c, seed);
 }
@@ -239,14 +262,14 @@ void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int 
 //  both:            the rotated query is rounded to the cache type.
 
 template <typename T>
-__global__ void k_ep_qkv(const float* __restrict__ raw, int ldr, const float* __restrict__ a, T* __restrict__ kvl,
-                         const float* __restrict__ rope, const Ctrl* __restrict__ ctrl, float* __restrict__ qatt,
-                         Couple C, int B, int lo, int Hq, int Hkv, int hd, int maxB, int max_len) {
+__global__ void k_ep_qkv(const float* __restrict__ raw, int ldr, const float* __restrict__ a, T* __restrict__ kv,
+                         int layer, KvMap km, const float* __restrict__ rope, const Ctrl* __restrict__ ctrl,
+                         float* __restrict__ qatt, Couple C, int B, int lo, int Hq, int Hkv, int hd) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   int m = lo + blockIdx.x;
   int f = m >= B, b = m - f * B;
-  int t = ctrl->t;
+  int t = kv_seq_pos(km, ctrl, b);
   int half = hd >> 1, qdim = Hq * hd, kvdim = Hkv * hd;
   const float* cs = rope + (size_t)t * hd;
   const float* rr = raw + (size_t)m * ldr;
@@ -273,18 +296,18 @@ __global__ void k_ep_qkv(const float* __restrict__ raw, int ldr, const float* __
     qatt[(size_t)m * qdim + n1] = Num<T>::quant(v1 * c + v0 * s);
   }
   if (f) return;
-  size_t vbase = (size_t)maxB * Hkv * max_len * hd;  // V half of the layer block
+  const int page = kv_page(km, b, t), off = kv_off(km, t);
   for (int p = threadIdx.x; p < Hkv * half; p += blockDim.x) {
     int g = p / half, i = p % half;
     float k0 = rr[qdim + g * hd + i], k1 = rr[qdim + g * hd + i + half];
     float c = cs[2 * i], s = cs[2 * i + 1];
-    T* Kp = kvl + (((size_t)b * Hkv + g) * max_len + t) * hd;
+    T* Kp = kv + kv_index(km, Hkv, hd, layer, 0, page, g, off);
     Kp[i] = Num<T>::from_f(k0 * c - k1 * s);
     Kp[i + half] = Num<T>::from_f(k1 * c + k0 * s);
   }
   for (int p = threadIdx.x; p < kvdim; p += blockDim.x) {
     int g = p / hd, i = p % hd;
-    T* Vp = kvl + vbase + (((size_t)b * Hkv + g) * max_len + t) * hd;
+    T* Vp = kv + kv_index(km, Hkv, hd, layer, 1, page, g, off);
     Vp[i] = Num<T>::from_f(rr[qdim + kvdim + p]);
   }
 }
@@ -293,14 +316,12 @@ void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, 
                    const Couple& C, const Rows& R, cudaStream_t s) {
   int n = R.hi - R.lo;
   if (n <= 0) return;
-  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
   if (D.bf16)
-    launch_pdl(k_ep_qkv<__nv_bfloat16>, dim3(n), dim3(256), 0, s, raw, ldr, a, (__nv_bfloat16*)kv + layer * layer_elems, Bf.rope,
-                                               Bf.ctrl, Bf.qatt, C, R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB,
-                                               D.max_len);
+    launch_pdl(k_ep_qkv<__nv_bfloat16>, dim3(n), dim3(256), 0, s, raw, ldr, a, (__nv_bfloat16*)kv, layer, Bf.kvm,
+               (const float*)Bf.rope, (const Ctrl*)Bf.ctrl, Bf.qatt, C, R.B, R.lo, D.Hq, D.Hkv, D.hd);
   else
-    launch_pdl(k_ep_qkv<float>, dim3(n), dim3(256), 0, s, raw, ldr, a, (float*)kv + layer * layer_elems, Bf.rope, Bf.ctrl, Bf.qatt, C,
-                                      R.B, R.lo, D.Hq, D.Hkv, D.hd, D.maxB, D.max_len);
+    launch_pdl(k_ep_qkv<float>, dim3(n), dim3(256), 0, s, raw, ldr, a, (float*)kv, layer, Bf.kvm,
+               (const float*)Bf.rope, (const Ctrl*)Bf.ctrl, Bf.qatt, C, R.B, R.lo, D.Hq, D.Hkv, D.hd);
 }
 
 // SwiGLU epilogue with the MLP-intermediate coupling ("Mecanismos Clave",
@@ -420,10 +441,10 @@ __device__ __forceinline__ void split_range(int n, int splits, int s, int& s0, i
 }
 
 template <typename T>
-__global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restrict__ qatt,
+__global__ void k_attn_generic(const T* __restrict__ kv, int layer, KvMap km, const float* __restrict__ qatt,
                                const Ctrl* __restrict__ ctrl, float* __restrict__ part_o,
-                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int maxB, int max_len,
-                               int splits, int flo, int fhi) {
+                               float* __restrict__ part_ml, int B, int Hkv, int G, int hd, int splits, int flo,
+                               int fhi) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   constexpr int CH = 128;  // positions per chunk == blockDim.x
@@ -437,11 +458,12 @@ __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restric
   float* mrow = sc + Ract * CH;         // [Ract]
   float* lrow = mrow + Ract;
   float* corr = lrow + Ract;
-  int n = ctrl->t + 1;
+  int n = kv_seq_pos(km, ctrl, b) + 1;
   int s0, s1;
   split_range(n, splits, s, s0, s1);
-  const T* K = kvl + ((size_t)b * Hkv + g) * max_len * hd;
-  const T* V = kvl + (size_t)maxB * Hkv * max_len * hd + ((size_t)b * Hkv + g) * max_len * hd;
+  // key/value row of position p of this (sequence, KV head)
+  auto Krow = [&](int p) { return kv + kv_index(km, Hkv, hd, layer, 0, kv_page(km, b, p), g, kv_off(km, p)); };
+  auto Vrow = [&](int p) { return kv + kv_index(km, Hkv, hd, layer, 1, kv_page(km, b, p), g, kv_off(km, p)); };
   float scale = 1.0f / sqrtf((float)hd);
   for (int idx = threadIdx.x; idx < Ract * hd; idx += blockDim.x) {
     int r = idx / hd, i = idx % hd;
@@ -458,7 +480,7 @@ __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restric
   for (int c0 = s0; c0 < s1; c0 += CH) {
     int pos = c0 + threadIdx.x;
     if (pos < s1) {
-      const T* kr = K + (size_t)pos * hd;
+      const T* kr = Krow(pos);
       for (int r = 0; r < Ract; ++r) {
         float dot = 0.f;
         for (int i = 0; i < hd; ++i) dot = fmaf(q[r * hd + i], Num<T>::to_f(kr[i]), dot);
@@ -493,7 +515,7 @@ __global__ void k_attn_generic(const T* __restrict__ kvl, const float* __restric
     for (int idx = threadIdx.x; idx < Ract * hd; idx += blockDim.x) {
       int r = idx / hd, i = idx % hd;
       float acc = o[idx] * corr[r];
-      for (int j = 0; j < cnt; ++j) acc = fmaf(sc[r * CH + j], Num<T>::to_f(V[(size_t)(c0 + j) * hd + i]), acc);
+      for (int j = 0; j < cnt; ++j) acc = fmaf(sc[r * CH + j], Num<T>::to_f(Vrow(c0 + j)[i]), acc);
       o[idx] = acc;
     }
     __syncthreads();
@@ -512,15 +534,14 @@ void launch_attention_generic(const Dims& D, const Buffers& Bf, const void* kv, 
   int Ract = (fhi - flo) * D.G;
   size_t smem = (size_t)(Ract * (2 * D.hd + 128) + 3 * Ract) * sizeof(float);
   dim3 grid(splits, D.Hkv, R.B);
-  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
   if (D.bf16) {
-    launch_pdl(k_attn_generic<__nv_bfloat16>, dim3(grid), dim3(128), smem, s, (const __nv_bfloat16*)kv + layer * layer_elems, Bf.qatt,
-                                                          Bf.ctrl, Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd,
-                                                          D.maxB, D.max_len, splits, flo, fhi);
+    launch_pdl(k_attn_generic<__nv_bfloat16>, dim3(grid), dim3(128), smem, s, (const __nv_bfloat16*)kv, layer,
+               Bf.kvm, (const float*)Bf.qatt, (const Ctrl*)Bf.ctrl, Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd,
+               splits, flo, fhi);
   } else {
-    launch_pdl(k_attn_generic<float>, dim3(grid), dim3(128), smem, s, (const float*)kv + layer * layer_elems, Bf.qatt, Bf.ctrl,
-                                                  Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd, D.maxB, D.max_len,
-                                                  splits, flo, fhi);
+    launch_pdl(k_attn_generic<float>, dim3(grid), dim3(128), smem, s, (const float*)kv, layer, Bf.kvm,
+               (const float*)Bf.qatt, (const Ctrl*)Bf.ctrl, Bf.part_o, Bf.part_ml, R.B, D.Hkv, D.G, D.hd, splits,
+               flo, fhi);
   }
 }
 
@@ -646,7 +667,7 @@ __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ l
                                                      float* __restrict__ logp_mix, int32_t* __restrict__ argmax,
                                                      float* __restrict__ alpha_out, float* __restrict__ logp1,
                                                      float* __restrict__ logp2, const Ctrl* __restrict__ ctrl,
-                                                     int32_t* __restrict__ sample_tok,
+                                                     KvMap km, int32_t* __restrict__ sample_tok,
                                                      int32_t* __restrict__ sample_hist, int hist_stride) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
@@ -704,7 +725,8 @@ __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ l
   const float lb = (alpha < 1.0f) ? log1pf(-alpha) : -INFINITY;
   const bool samp = sample_tok != nullptr;
   const unsigned long long seed = samp ? ctrl->seed : 0ull;
-  const int tpos = samp ? ctrl->t : 0;
+  const int tpos = samp ? kv_seq_pos(km, ctrl, b) : 0;
+  const int hrow = samp ? ctrl->gen_row : 0;
   float best = -INFINITY, sbest = -INFINITY;
   int bi = 0x7fffffff, sbi = 0x7fffffff;
   const int jb0 = (v0 + 3) >> 2, jb1 = (v1 + 3) >> 2;
@@ -771,7 +793,7 @@ __global__ void __launch_bounds__(kMixThreads) k_mix(const float* __restrict__ l
     if (alpha_out) alpha_out[b] = alpha;
     if (samp) {
       sample_tok[b] = si;
-      if (sample_hist) sample_hist[(size_t)tpos * hist_stride + b] = si;
+      if (sample_hist) sample_hist[(size_t)hrow * hist_stride + b] = si;
     }
   }
   // keep every CTA's shared memory alive until rank 0 has read it
@@ -795,7 +817,7 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
   lc.attrs = at;
   lc.numAttrs = 2;
   cudaLaunchKernelEx(&lc, k_mix, (const float*)Bf.logits, B, D.V, aux_on, logp_mix, argmax, alpha, logp1, logp2,
-                     (const Ctrl*)Bf.ctrl, sample_tok, sample_hist, D.maxB);
+                     (const Ctrl*)Bf.ctrl, Bf.kvm, sample_tok, sample_hist, D.maxB);
 }
 
 // ------------------------------------------------------------------ MoE (router replay)

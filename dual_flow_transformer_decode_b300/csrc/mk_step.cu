@@ -1291,6 +1291,7 @@ bool mk_eligible(const Dims& D, std::string* why) {
   };
   if (!D.bf16) return no("not bf16");
   if (D.E) return no("MoE model");
+  if (D.paged) return no("paged KV cache");
   if (D.hd != kHD) return no("head_dim is not 128");
   if (D.G > 4) return no("more than 4 query heads per KV head");
   if (D.d % kBM || D.d > 8192) return no("d_model not a multiple of 128 (or above 8192)");

@@ -62,9 +62,11 @@ struct BpEp {
   int Mc, C, p0;        // rows of the chunk, positions per sequence in it, first position
   __nv_bfloat16* q;     // [rows][qdim] rotated queries
   int qdim, kvdim;
-  __nv_bfloat16* kK;    // layer K block of the cache [maxB][Hkv][max_len][hd]
-  __nv_bfloat16* kV;    // layer V block
-  int Hkv, max_len;
+  __nv_bfloat16* kv;    // the cache (all layers)
+  int layer;
+  KvMap km;             // cache addressing
+  int slot0;            // cache sequence of the chunk's sequence 0
+  int Hkv;
   const float* rope;    // [max_len][hd/2][2]
   float* h;             // residual rows [rows][d]
   int d;
@@ -217,14 +219,16 @@ __global__ void __launch_bounds__(128, 1)
             store16(qr + 16 * c, ra);
             store16(qr + 64 + 16 * c, rb);
           } else {
-            const int g = (n0 - ep.qdim) / kHD;
-            __nv_bfloat16* K = ep.kK + (((size_t)b * ep.Hkv + g) * ep.max_len + pos) * kHD;
+            const int g = (n0 - ep.qdim) / kHD, sq = ep.slot0 + b;
+            __nv_bfloat16* K =
+                ep.kv + kv_index(ep.km, ep.Hkv, kHD, ep.layer, 0, kv_page(ep.km, sq, pos), g, kv_off(ep.km, pos));
             store16(K + 16 * c, ra);
             store16(K + 64 + 16 * c, rb);
           }
         } else {
-          const int g = (n0 - ep.qdim - ep.kvdim) / kHD;
-          __nv_bfloat16* V = ep.kV + (((size_t)b * ep.Hkv + g) * ep.max_len + pos) * kHD;
+          const int g = (n0 - ep.qdim - ep.kvdim) / kHD, sq = ep.slot0 + b;
+          __nv_bfloat16* V =
+              ep.kv + kv_index(ep.km, ep.Hkv, kHD, ep.layer, 1, kv_page(ep.km, sq, pos), g, kv_off(ep.km, pos));
           store16(V + 16 * c, lo);
           store16(V + 64 + 16 * c, hi);
         }
@@ -293,8 +297,8 @@ __device__ __forceinline__ uint32_t sw_off(int pos, int dim) {
 // row b*C + i holds position p0 + i of sequence b.
 __global__ void __launch_bounds__(160, 1)
     k_bp_attn(const __grid_constant__ CUtensorMap tkv, const __nv_bfloat16* __restrict__ q,
-              __nv_bfloat16* __restrict__ o, Ctrl* __restrict__ ctrl, int layer, int maxB, int Hkv, int G,
-              int qdim, int C, int p0) {
+              __nv_bfloat16* __restrict__ o, Ctrl* __restrict__ ctrl, int layer, KvMap km, int slot0, int Hkv,
+              int G, int qdim, int C, int p0) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + ANS * ASTAGE);
@@ -306,7 +310,10 @@ __global__ void __launch_bounds__(160, 1)
   const int nq = min(TP, C - i0);
   const int kend = p0 + i0 + nq;  // keys [0, kend): the cache up to the block's last query
   const int ntiles = (kend + TP - 1) / TP;
-  const int zK = ((layer * 2) * maxB + b) * Hkv + g, zV = ((layer * 2 + 1) * maxB + b) * Hkv + g;
+  // tensor-map rows of the K / V blocks of the page holding key position p
+  // (a 64-position tile never spans two pages), and its offset there
+  const int sq = slot0 + b;
+  auto tile_z = [&](int p, int kvsel) { return ((layer * 2 + kvsel) * km.NP + kv_page(km, sq, p)) * Hkv + g; };
   if (tid == 0) {
     for (int i = 0; i < ANS; ++i) {
       ptx::mbar_init(&full[i], 1);
@@ -331,12 +338,13 @@ __global__ void __launch_bounds__(160, 1)
           break;
         }
         if (*abort_flag) break;
+        const int kp = i * TP, zK = tile_z(kp, 0), zV = tile_z(kp, 1), y = kv_off(km, kp);
         uint8_t* dst = ring + st * ASTAGE;
         ptx::mbar_arrive_expect_tx(&full[st], ASTAGE);
-        ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[st], 0, i * TP, zK);
-        ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[st], 64, i * TP, zK);
-        ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[st], 0, i * TP, zV);
-        ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[st], 64, i * TP, zV);
+        ptx::tma_load_3d(dst + 0 * BOX, &tkv, &full[st], 0, y, zK);
+        ptx::tma_load_3d(dst + 1 * BOX, &tkv, &full[st], 64, y, zK);
+        ptx::tma_load_3d(dst + 2 * BOX, &tkv, &full[st], 0, y, zV);
+        ptx::tma_load_3d(dst + 3 * BOX, &tkv, &full[st], 64, y, zV);
         issued = i + 1;
       }
       if (*abort_flag)
@@ -589,9 +597,8 @@ bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err) {
 
 void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dims& D, const Buffers& Bf,
                 void* kv, const void* emb1, const float* const* attn_norm, const float* const* mlp_norm,
-                const int32_t* tokens, int B, int n, cudaStream_t s) {
+                const int32_t* tokens, int B, int n, int slot0, cudaStream_t s) {
   const int C = std::max(1, P.mcap / B);
-  const size_t kvs = (size_t)D.maxB * D.Hkv * D.max_len * D.hd;
   __nv_bfloat16* kvb = static_cast<__nv_bfloat16*>(kv);
   for (int p0 = 0; p0 < n; p0 += C) {
     const int Ce = std::min(C, n - p0), Mc = B * Ce;
@@ -605,20 +612,21 @@ void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dim
     ep.qdim = D.qdim;
     ep.kvdim = D.kvdim;
     ep.Hkv = D.Hkv;
-    ep.max_len = D.max_len;
+    ep.kv = kvb;
+    ep.km = Bf.kvm;
+    ep.slot0 = slot0;
     ep.rope = Bf.rope;
     ep.h = P.h;
     ep.d = D.d;
     ep.z = static_cast<__nv_bfloat16*>(P.z);
     ep.F = D.F;
     for (int l = 0; l < D.L; ++l) {
-      ep.kK = kvb + (size_t)l * 2 * kvs;
-      ep.kV = ep.kK + kvs;
+      ep.layer = l;
       launch_rmsnorm_rows(D, P.h, attn_norm[l], P.u, Mc, s);
       ep.op = BP_QKV;
       gemm(P.x_u, tc.w_qkv[l], D.d, D.qkvn, ep, Bf.ctrl, s);
       launch_ex(k_bp_attn, dim3((Ce + TP - 1) / TP, D.Hq, B), dim3(160), attn_smem(), s, at.kv,
-                static_cast<const __nv_bfloat16*>(P.q), static_cast<__nv_bfloat16*>(P.o), Bf.ctrl, l, D.maxB,
+                static_cast<const __nv_bfloat16*>(P.q), static_cast<__nv_bfloat16*>(P.o), Bf.ctrl, l, Bf.kvm, slot0,
                 D.Hkv, D.G, D.qdim, Ce, p0);
       ep.op = BP_RESID;
       gemm(P.x_o, tc.w_o[l], D.qdim, D.d, ep, Bf.ctrl, s);

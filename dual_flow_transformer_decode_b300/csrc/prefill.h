@@ -31,10 +31,12 @@ size_t bp_workspace_bytes(const Dims& D);
 // Carves the chunk buffers from `region` and encodes their tensor maps.
 bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err);
 // Prefill positions [0, n) of B sequences (primary flow only): tokens is a
-// device [B][n] array of ids.  Every layer runs once per chunk of positions;
-// the KV cache receives positions 0..n-1.  Enqueued on `s`.
+// device [B][n] array of ids; sequence i of the call is cache sequence
+// slot0 + i.  Every layer runs once per chunk of positions; the KV cache
+// receives positions 0..n-1 (paged mode: into the pages the table already
+// lists for them).  Enqueued on `s`.
 void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dims& D, const Buffers& Bf,
                 void* kv, const void* emb1, const float* const* attn_norm, const float* const* mlp_norm,
-                const int32_t* tokens, int B, int n, cudaStream_t s);
+                const int32_t* tokens, int B, int n, int slot0, cudaStream_t s);
 
 }  // namespace df

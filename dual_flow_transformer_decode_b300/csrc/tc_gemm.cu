@@ -56,11 +56,13 @@ struct EpArgs {
   int n_out;      // valid output features of the matrix
   // QKV
   const float* a;
-  __nv_bfloat16* kvl;  // layer block of the cache
+  __nv_bfloat16* kv;   // the cache (all layers)
+  int layer;
+  KvMap km;            // cache addressing; paged mode: per-sequence positions
   const float* rope;
   const Ctrl* ctrl;
   float* qatt;
-  int qdim, kvdim, hd, Hkv, maxB, max_len;
+  int qdim, kvdim, hd, Hkv;
   // couplings
   Couple C;
   const float* bvec;
@@ -149,16 +151,27 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
   const int np = p1 - p0;
   const bool prim = ep.lo < ep.B, aux = ep.hi > ep.B;
   const int B = ep.B;
-  const int t = ep.op == (int)TcOp::QKV ? ep.ctrl->t : 0;
+  // paged mode: every sequence at its own position, so the RoPE angles are
+  // read per unit instead of from the staged table
+  const bool ragged = ep.km.table != nullptr;
+  const int t = ep.op == (int)TcOp::QKV && !ragged ? ep.ctrl->t : 0;
   for (int u = tid; u < B * np; u += nthreads) {
     const int b = u / np, pp = u % np, p = p0 + pp;
     Pair v1{0.f, 0.f}, v2{0.f, 0.f};
     if (prim) v1 = reduce_pair(cl, st, S, b, p);
     if (aux) v2 = reduce_pair(cl, st, S, B + b, p);
     const int g0 = n0 + p, g1 = n0 + p + 64;
-    const float c = par[pp], sn = par[64 + pp], cx = par[128 + pp], cy = par[192 + pp];
+    float c = par[pp], sn = par[64 + pp];
+    const float cx = par[128 + pp], cy = par[192 + pp];
     switch (ep.op) {
       case (int)TcOp::QKV: {
+        int tb = t;
+        if (ragged) {
+          tb = ep.km.pos[b];
+          const float* cs = ep.rope + (size_t)tb * ep.hd;
+          c = cs[2 * p];
+          sn = cs[2 * p + 1];
+        }
         if (n0 < ep.qdim) {
           if (prim) {
             if (ep.C.save) {
@@ -185,8 +198,8 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
         } else if (prim) {
           const bool isk = n0 < ep.qdim + ep.kvdim;
           const int g = (isk ? n0 - ep.qdim : n0 - ep.qdim - ep.kvdim) / ep.hd;
-          const size_t vofs = isk ? 0 : (size_t)ep.maxB * ep.Hkv * ep.max_len * ep.hd;
-          __nv_bfloat16* P = ep.kvl + vofs + (((size_t)b * ep.Hkv + g) * ep.max_len + t) * ep.hd;
+          __nv_bfloat16* P = ep.kv + kv_index(ep.km, ep.Hkv, ep.hd, ep.layer, isk ? 0 : 1, kv_page(ep.km, b, tb), g,
+                                              kv_off(ep.km, tb));
           if (isk) {
             P[p] = __float2bfloat16_rn(v1.lo * c - v1.hi * sn);
             P[p + 64] = __float2bfloat16_rn(v1.hi * c + v1.lo * sn);
@@ -556,8 +569,7 @@ EpArgs base_args(const Dims& D, const Buffers& Bf, const Rows& R, TcOp op, int n
   ep.kvdim = D.kvdim;
   ep.hd = D.hd;
   ep.Hkv = D.Hkv;
-  ep.maxB = D.maxB;
-  ep.max_len = D.max_len;
+  ep.km = Bf.kvm;
   ep.h = Bf.h;
   ep.d = D.d;
   ep.z = (__nv_bfloat16*)Bf.z;
@@ -605,8 +617,8 @@ void tc_qkv(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, co
   EpArgs ep = base_args(D, Bf, R, TcOp::QKV, D.qkvn);
   ep.a = a;
   ep.C = C;
-  size_t layer_elems = (size_t)2 * D.maxB * D.Hkv * D.max_len * D.hd;
-  ep.kvl = (__nv_bfloat16*)kv + layer * layer_elems;
+  ep.kv = (__nv_bfloat16*)kv;
+  ep.layer = layer;
   launch(P, P.w_qkv[layer], P.x_u, D.qkvn, D.d, ep, Bf, s, P.splits[(int)TcOp::QKV]);
 }
 

@@ -29,7 +29,10 @@ class DualFlowModel:
     """
 
     def __init__(self, cfg, weights, max_batch: int | None = None, max_len: int | None = None,
-                 device: str | torch.device = "cuda", stream: torch.cuda.Stream | None = None):
+                 device: str | torch.device = "cuda", stream: torch.cuda.Stream | None = None,
+                 page_len: int = 0, n_pages: int = 0):
+        """page_len > 0: paged KV cache of n_pages pages (per-sequence
+        lengths; see prefill_seq / release_seq)."""
         self.cfg = cfg
         self.device = torch.device(device)
         self.max_batch = max_batch or cfg.batch
@@ -37,7 +40,8 @@ class DualFlowModel:
         self.dtype = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
         self.stream = stream or torch.cuda.current_stream(self.device)
         self._keep = []
-        self.c_cfg = _b.make_config(cfg, self.max_batch, self.max_len)
+        self.page_len, self.n_pages = page_len, n_pages
+        self.c_cfg = _b.make_config(cfg, self.max_batch, self.max_len, page_len, n_pages)
         ws_bytes, kv_bytes = _b.df_workspace_bytes(self.c_cfg)
         if ws_bytes == 0:
             raise _b.DFError(_b.DF_ERR_ARG, "invalid configuration")
@@ -102,6 +106,26 @@ class DualFlowModel:
     def set_length(self, B: int, t: int) -> None:
         _b.df_set_length(self.ctx, B, t)
 
+    # ------------------------------------------------------------- paged cache
+    def set_batch(self, B: int) -> None:
+        _b.df_set_batch(self.ctx, B)
+
+    def prefill_seq(self, b: int, tokens: torch.Tensor) -> None:
+        """Prefill slot b with its own prompt (device int32 [n])."""
+        assert tokens.dtype == torch.int32 and tokens.is_cuda and tokens.is_contiguous() and tokens.dim() == 1
+        self._keep_seq = getattr(self, "_keep_seq", {})
+        self._keep_seq[b] = tokens
+        _b.df_prefill_seq(self.ctx, b, tokens.data_ptr(), tokens.numel())
+
+    def release_seq(self, b: int) -> None:
+        _b.df_release_seq(self.ctx, b)
+
+    def seq_lengths(self) -> list[int]:
+        return _b.df_seq_lengths(self.ctx, self.max_batch)
+
+    def seq_pages(self, b: int) -> list[int]:
+        return _b.df_seq_pages(self.ctx, b)
+
     def decode_step(self, tokens: torch.Tensor, logp_mix: torch.Tensor | None = None,
                     argmax: torch.Tensor | None = None, alpha: torch.Tensor | None = None) -> None:
         assert tokens.dtype == torch.int32 and tokens.is_cuda
@@ -150,10 +174,24 @@ class DualFlowModel:
         return _b.df_step_kernels(self.ctx)
 
     def kv_view(self) -> torch.Tensor:
-        """The KV cache as [L][2][max_batch][Hkv][max_len][hd] (a view, no copy)."""
+        """The KV cache as [L][2][max_batch][Hkv][max_len][hd] (a view, no
+        copy); paged mode: [L][2][n_pages + 1][Hkv][page_len][hd]."""
         cfg = self.cfg
+        if self.page_len:
+            return self.kv.view(self.dtype).view(cfg.n_layers, 2, self.n_pages + 1, cfg.n_kv_heads, self.page_len,
+                                                 cfg.head_dim)
         return self.kv.view(self.dtype).view(cfg.n_layers, 2, self.max_batch, cfg.n_kv_heads, self.max_len,
                                              cfg.head_dim)
+
+    def seq_kv(self, b: int) -> torch.Tensor:
+        """Paged mode: slot b's cache gathered as [L][2][Hkv][length][hd] (a copy)."""
+        kv = self.kv_view()
+        n = self.seq_lengths()[b]
+        pages = self.seq_pages(b)
+        parts = [kv[:, :, p] for p in pages]
+        if not parts:
+            return kv[:, :, 0, :, :0]
+        return torch.cat(parts, dim=3)[:, :, :, :n]
 
     def close(self) -> None:
         if getattr(self, "ctx", None):

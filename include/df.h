@@ -66,6 +66,13 @@ typedef struct {
                               logits among the other experts (0 = top_k).
                               Prefill cost is unchanged; decode reads the
                               extra experts' weights once for the batch.   */
+  int page_len;            /* 0: contiguous KV cache, every sequence of the
+                              batch at one common position.  A power of two
+                              >= 64: paged KV cache with per-sequence
+                              lengths (ragged batches, slots filled and
+                              released between steps; see df_prefill_seq).  */
+  int n_pages;             /* paged mode: pages of page_len positions in the
+                              pool shared by all sequences (>= 1)           */
 } df_config;
 
 /* Parameter set (all device pointers; the struct and its per-layer arrays
@@ -214,10 +221,54 @@ df_status df_debug_outputs(df_ctx* ctx, float* logp1, float* logp2, int32_t* top
 df_status df_decode_step_noalloc(df_ctx* ctx, const int32_t* tokens, float* logp_mix, int32_t* argmax,
                                  float* alpha);
 
+/* ---- Paged KV cache: ragged batches and continuous decode -------------
+ *
+ * With page_len > 0 the cache is a pool of n_pages pages, each holding
+ * page_len positions of one sequence for every layer and KV head
+ * ([n_layers][2][n_pages + 1][n_kv_heads][page_len][head_dim]; the last page
+ * is a sink that free slots write into).  Every sequence (slot b of the
+ * batch) has its own length: a decode step processes each active slot at its
+ * own position t_b (RoPE angle, cache slot and attention range 0..t_b; the
+ * draw of df_generate uses t_b too), so the result for a slot is the one a
+ * batch of that sequence alone would give ("Arquitectura Central": one
+ * persistent primary cache per sequence; the auxiliary flow reads it at the
+ * same position).  Pages are taken from the pool when a slot's next position
+ * starts a page and returned when the slot is released or prefilled again.
+ * df_prefill and df_set_length prefill / declare all B slots with one length;
+ * the calls below manage single slots.  Steps decode the slots [0, B) of the
+ * last df_set_batch / df_prefill / df_set_length: free slots are computed
+ * too, their outputs are unspecified and nothing of theirs is kept.  A step
+ * returns DF_ERR_CAPACITY, with nothing enqueued, when an active slot would
+ * pass max_len or the pool has no page for a position it must write. */
+
+/* Paged mode: decode B slots per step from now on; slots >= B are released,
+ * slots < B keep their sequences.  DF_ERR_UNSUPPORTED in contiguous mode. */
+df_status df_set_batch(df_ctx* ctx, int B);
+
+/* Paged mode: prefill slot b (0 <= b < B) with its own prompt of n
+ * positions (tokens: device int32 [n]), primary flow only; the slot's old
+ * sequence, if any, is released first.  The next decode step processes the
+ * slot at position n.  Other slots are unchanged.  DF_ERR_CAPACITY (slot
+ * left as it was) when the pool cannot hold n positions. */
+df_status df_prefill_seq(df_ctx* ctx, int b, const int32_t* tokens, int n);
+
+/* Paged mode: release slot b, returning its pages to the pool. */
+df_status df_release_seq(df_ctx* ctx, int b);
+
+/* Length of every slot (host int32 [max_batch]): -1 for free slots and slots
+ * >= B.  Contiguous mode: the common length for b < B. */
+df_status df_seq_lengths(const df_ctx* ctx, int32_t* lengths);
+
+/* Paged mode: the physical pages of slot b in logical order (host int32,
+ * up to cap written); returns the slot's page count, -1 on a bad argument
+ * or in contiguous mode. */
+int df_seq_pages(const df_ctx* ctx, int b, int32_t* pages, int cap);
+
 /* Synchronise the stream and report any latched device error. */
 df_status df_sync(df_ctx* ctx);
 
-/* Current position (number of valid cache positions). */
+/* Current position (number of valid cache positions); paged mode: the
+ * largest length among the active slots. */
 int df_length(const df_ctx* ctx);
 
 /* Number of kernels in the last captured step graph (decode or prefill
