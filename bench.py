@@ -207,28 +207,57 @@ def run_ours(args, rank, world, local_rank):
     B, P = cfg.batch, cfg.n_prefill
     K, W = args.steps, args.warmup
     span = max(cfg.n_steps, W + K)
-    max_len = P + span
+    # per-sequence prompt lengths (all P unless the workload is ragged); the
+    # decode steps of sequence b read tokens lens[b], lens[b] + 1, ...
+    lens = dfsynth.prompt_lengths(cfg, args.seed + rank)
+    max_len = int(lens.max()) + span
     tok = dfsynth.tokens(cfg.with_(n_steps=span), args.seed + rank)
+    paged = cfg.page_len > 0
+    n_pages = int(sum((int(n) + span + cfg.page_len - 1) // cfg.page_len for n in lens)) if paged else 0
     model = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, args.seed, dev), max_batch=B, max_len=max_len,
-                          device=dev)
+                          device=dev, page_len=cfg.page_len, n_pages=n_pages)
     tok_d = torch.from_numpy(tok).to(dev)
+    P_mean = float(lens.mean())
+
+    def prefill_all():
+        if paged:
+            model.set_batch(B)
+            for b in range(B):
+                model.prefill_seq(b, tok_d[b, :int(lens[b])].contiguous())
+        else:
+            model.prefill(tok_d[:, :P].contiguous())
+
+    def reset(t=None):
+        """Back to position t (default P, the end of the prompt).  Paged: every
+        slot is prefilled again to its own prompt length and then decoded
+        t - P steps, so each sequence stands t - P positions past its prompt."""
+        if paged:
+            prefill_all()
+            for s in range((P if t is None else t) - P):
+                step(s)
+        else:
+            model.set_length(B, P if t is None else t)
+
     prefill = None
     if args.quick:
-        model.set_length(B, P)   # timing-only: cache contents do not change the work
+        if paged:
+            prefill_all()
+        else:
+            model.set_length(B, P)   # timing-only: cache contents do not change the work
     else:
         # prefill of the prompt (primary flow only), timed once with CUDA events
-        prompt = tok_d[:, :P].contiguous()
         model.sync()
         p0 = torch.cuda.Event(enable_timing=True)
         p1 = torch.cuda.Event(enable_timing=True)
         p0.record(model.stream)
-        model.prefill(prompt)
+        prefill_all()
         p1.record(model.stream)
         model.sync()
         pms = p0.elapsed_time(p1)
-        flop = prefill_flops(cfg, B, P)
+        flop = sum(prefill_flops(cfg, 1, int(n)) for n in lens)
         bf16_peak = _bf16_sustained()  # the prefill runs for tens of milliseconds
-        prefill = {"positions": P, "batch": B, "ms": round(pms, 3), "tokens_per_s": round(B * P / (pms / 1e3), 1),
+        prefill = {"positions": P if not cfg.ragged else int(lens.sum()) // B, "batch": B, "ms": round(pms, 3),
+                   "tokens_per_s": round(float(lens.sum()) / (pms / 1e3), 1),
                    "algorithmic_tflop": round(flop / 1e12, 3),
                    "achieved_tflops": round(flop / (pms / 1e3) / 1e12, 1),
                    "peak_tflops": bf16_peak, "peak_kind": "measured bf16 sustained",
@@ -236,7 +265,9 @@ def run_ours(args, rank, world, local_rank):
                    "path": "serial" if os.environ.get("DF_SERIAL_PREFILL") == "1" or cfg.n_experts or
                    cfg.dtype != "bf16" else "batched"}
     model.sync()
-    steps_tok = tok_d[:, P:].t().contiguous()          # [span][B]
+    # [span][B]: step s feeds sequence b its token at position lens[b] + s
+    steps_idx = torch.from_numpy(lens[None, :] + np.arange(span)[:, None]).to(dev)
+    steps_tok = torch.gather(tok_d.t(), 0, steps_idx).contiguous()
     # The step graph is cached per (token buffer, output buffers): feed each
     # step's ids through one fixed buffer, as a serving loop would.
     tok_buf = torch.empty(B, dtype=torch.int32, device=dev)
@@ -285,7 +316,8 @@ def run_ours(args, rank, world, local_rank):
     kernels = model.step_kernels
     ms_step = ms_total / K
     tokens_s = world * B * K / (ms_total / 1e3)
-    t_mid = P + W + K // 2
+    t_mid = P + W + K // 2           # mean position of the timed steps (ragged: offset from the mean prompt)
+    t_mean = int(round(P_mean)) + W + K // 2
     if args.quick:
         model.close()
         return {"metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 4),
@@ -299,7 +331,7 @@ def run_ours(args, rank, world, local_rank):
         ka = max(cfg.aux_k, cfg.top_k)
         tk = torch.zeros(cfg.n_layers, B, ka, dtype=torch.int32, device=dev)
         model.debug_outputs(topk=tk)
-        model.set_length(B, t_mid)
+        reset(t_mid)
         step(0)
         model.sync()
         tkh = tk.cpu().numpy()
@@ -308,7 +340,7 @@ def run_ours(args, rank, world, local_rank):
         model.debug_outputs()
 
     # per-step latency distribution: an event pair around every step
-    model.set_length(B, P)
+    reset()
     for s in range(min(W, 3)):
         step(s)
     n_lat = min(K, 64)
@@ -326,25 +358,25 @@ def run_ours(args, rank, world, local_rank):
     # ablations on the same positions: two ungrouped passes, and primary-only decode
     abl = {}
     for name, aux, ung in (("ungrouped_two_pass", 1, 1), ("aux_off_standard_decode", 0, 0)):
-        model.set_length(B, P)
+        reset()
         model.set_mode(aux, ung)
         kk = min(K, 32)
         ms = max_over_ranks(timed(min(W, 3), kk)) / kk
         abl[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * B / (ms / 1e3), 1),
                      # two passes each read every weight and the whole cache (the
                      # auxiliary pass its own experts too); primary-only reads them once
-                     "algorithmic_bytes": step_bytes(cfg, B, t_mid, moe_union_primary) +
-                     step_bytes(cfg, B, t_mid, moe_union) if ung
-                     else step_bytes(cfg, B, t_mid, moe_union_primary)}
+                     "algorithmic_bytes": step_bytes(cfg, B, t_mean, moe_union_primary) +
+                     step_bytes(cfg, B, t_mean, moe_union) if ung
+                     else step_bytes(cfg, B, t_mean, moe_union_primary)}
     model.set_mode(1, 0)
 
     # generation: the same positions, each step fed the token drawn from
     # p_mix at the step before (one df_generate call for all K steps)
     gen_out = torch.empty(max(K, 3), B, dtype=torch.int32, device=dev)
     tok_buf.copy_(steps_tok[0])
-    model.set_length(B, P)
+    reset()
     model.generate(tok_buf, min(W, 3), args.seed, gen_out)  # warm-up (captures the step graph)
-    model.set_length(B, P)
+    reset()
     tok_buf.copy_(steps_tok[0])
     torch.cuda.synchronize(dev)
     barrier()
@@ -361,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
                   "steps": K, "draw": "Gumbel-max over Philox4x64-10 noise, fed back on the device"}
 
     # dominant operation: time every op, cycling layers, with CUDA events
-    model.set_length(B, t_mid)
+    reset(t_mid)
     step(0)
     ops = ["qkv", "attn", "wo"] + (["moe"] if cfg.n_experts else ["gateup", "down"]) + ["lmhead"]
     per_step_count = {o: (1 if o == "lmhead" else cfg.n_layers) for o in ops}
@@ -372,18 +404,18 @@ def run_ours(args, rank, world, local_rank):
     shares = {o: op_ms[o] * per_step_count[o] for o in ops}
     dom = max(shares, key=shares.get)
     hbm_peak, _, peak_kind = _peaks()
-    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mid + 1, moe_union)
+    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mean + 1, moe_union)
     achieved = bytes_dom / (op_ms[dom] / 1e3) / 1e9
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": captured_traffic(cfg.name, dom),
                 "peak_source": peak_kind, "ms_per_launch": round(op_ms[dom], 5),
                 "algorithmic_bytes_per_launch": bytes_dom}
-    sb = step_bytes(cfg, B, t_mid, moe_union)
+    sb = step_bytes(cfg, B, t_mean, moe_union)
     step_gbs = sb / (ms_step / 1e3) / 1e9
 
     # end to end through the host-buffer entry point (pinned host memory)
-    model.set_length(B, P)
-    h_tok = torch.from_numpy(tok[:, P:].T.copy()).pin_memory()
+    reset()
+    h_tok = steps_tok.cpu().pin_memory()
     h_lp = torch.empty(B, cfg.vocab).pin_memory()
     h_am = torch.empty(B, dtype=torch.int32).pin_memory()
     h_al = torch.empty(B).pin_memory()
@@ -404,7 +436,10 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(tokens_s, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": B, "stacked_rows": 2 * B, "context_at_first_step": P,
+        "config": {"workload": cfg.name, "batch": B, "stacked_rows": 2 * B,
+                   "context_at_first_step": P if not cfg.ragged else
+                   {"min": int(lens.min()), "mean": round(P_mean, 1), "max": int(lens.max())},
+                   "kv_cache": f"paged, {cfg.page_len} positions per page" if paged else "contiguous",
                    "layers": cfg.n_layers, "d_model": cfg.d_model, "vocab": cfg.vocab,
                    "experts": cfg.n_experts, "l2": "inputs larger than L2 (weights + KV per step >> 126 MB)",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},

@@ -12,6 +12,7 @@ from .gen import (  # noqa: F401
     Weights,
     DeviceWeights,
     tokens,
+    prompt_lengths,
     synthetic_kv_block,
     bf16_round_f32,
     tensor_id,

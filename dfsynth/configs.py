@@ -45,10 +45,16 @@ class DFConfig:
     router_std: float = -1.0  # <0 means 1/sqrt(d_model)
     lm_scale: float = 1.0    # multiplies the LM-head draw (peaked-logit tests)
     aux_top_k: int = 0       # MoE auxiliary fan-out (0: the auxiliary flow replays the primary's top_k)
+    page_len: int = 0        # >0: paged KV cache with pages of this many positions
+    ragged: float = 0.0      # >0: prompt lengths uniform in n_prefill * [1 - ragged, 1 + ragged]
+
+    @property
+    def max_prompt(self) -> int:
+        return int(round(self.n_prefill * (1.0 + self.ragged)))
 
     @property
     def max_len(self) -> int:
-        return self.n_prefill + self.n_steps
+        return self.max_prompt + self.n_steps
 
     @property
     def q_dim(self) -> int:
@@ -147,6 +153,11 @@ VARIANTS = {
     # the MoE workload with the auxiliary flow using 8 experts per token
     # (4 replayed + 4 of its own): decode compute grows, prefill does not
     "moe64e_top4_aux8": WORKLOADS["moe64e_top4"].with_(name="moe64e_top4_aux8", aux_top_k=8),
+    # the headline model over a paged cache (64-position pages): every
+    # sequence at the same length, then a ragged batch whose prompt lengths
+    # are uniform in [512, 1535] (mean ~1023, as the headline workload)
+    "dense1b_paged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_paged", page_len=64),
+    "dense1b_ragged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_ragged", page_len=64, ragged=0.5),
 }
 
 

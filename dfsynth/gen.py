@@ -28,6 +28,7 @@ _LAYER_SLOTS = {"attn_norm": 0, "wq": 1, "wk": 2, "wv": 3, "wo": 4, "mlp_norm": 
 _EXPERT_SLOTS = {"wg": 0, "wu": 1, "wd": 2}
 _GLOBAL_IDS = {"emb1": 2, "emb2": 3, "lm_head": 4, "final_norm": 5}
 TOKENS_ID = 1
+LENGTHS_ID = 6
 
 
 def bf16_round_f32(x: np.ndarray) -> np.ndarray:
@@ -154,10 +155,23 @@ class Weights:
 
 
 def tokens(cfg, seed: int = 0, batch: int | None = None) -> np.ndarray:
-    """Token ids int32[B][n_prefill + n_steps], uniform over the vocabulary."""
+    """Token ids int32[B][max_prompt + n_steps], uniform over the vocabulary
+    (max_prompt = n_prefill unless the workload's prompts are ragged)."""
     B = cfg.batch if batch is None else batch
     g = _rng(seed, TOKENS_ID)
-    return g.integers(0, cfg.vocab, size=(B, cfg.n_prefill + cfg.n_steps), dtype=np.int64).astype(np.int32)
+    return g.integers(0, cfg.vocab, size=(B, cfg.max_prompt + cfg.n_steps), dtype=np.int64).astype(np.int32)
+
+
+def prompt_lengths(cfg, seed: int = 0, batch: int | None = None) -> np.ndarray:
+    """Prompt length of each sequence: n_prefill for every sequence, or for a
+    ragged workload uniform integers in [n_prefill (1 - ragged),
+    n_prefill (1 + ragged)] (seeded)."""
+    B = cfg.batch if batch is None else batch
+    if not cfg.ragged:
+        return np.full(B, cfg.n_prefill, dtype=np.int64)
+    lo = int(round(cfg.n_prefill * (1.0 - cfg.ragged)))
+    g = _rng(seed, LENGTHS_ID)
+    return g.integers(lo, cfg.max_prompt + 1, size=B, dtype=np.int64)
 
 
 def synthetic_kv_block(cfg, seed: int, layer: int, b: int, n_pos: int, std: float = 1.0):
