@@ -109,14 +109,12 @@ class Clocks:
 
 # Source files of each operation's kernels; an ncu figure is used only while
 # these files are unchanged since the capture.
+_CS = "dual_flow_transformer_decode_b300/csrc/"
+_GEMM = [_CS + "tc_gemm.cu", _CS + "ptx.cuh", _CS + "common.cuh"]
 OP_SOURCES = {
-    "gateup": ["dual_flow_transformer_decode_b300/csrc/tc_gemm.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "down": ["dual_flow_transformer_decode_b300/csrc/tc_gemm.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "qkv": ["dual_flow_transformer_decode_b300/csrc/tc_gemm.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "wo": ["dual_flow_transformer_decode_b300/csrc/tc_gemm.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "lmhead": ["dual_flow_transformer_decode_b300/csrc/tc_gemm.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "attn": ["dual_flow_transformer_decode_b300/csrc/attn_fast.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
-    "moe": ["dual_flow_transformer_decode_b300/csrc/tc_moe.cu", "dual_flow_transformer_decode_b300/csrc/ptx.cuh"],
+    "gateup": _GEMM, "down": _GEMM, "qkv": _GEMM, "wo": _GEMM, "lmhead": _GEMM,
+    "attn": [_CS + "attn_fast.cu", _CS + "ptx.cuh", _CS + "common.cuh"],
+    "moe": [_CS + "tc_moe.cu", _CS + "kernels_basic.cu", _CS + "ptx.cuh", _CS + "common.cuh"],
 }
 
 

@@ -126,3 +126,67 @@ def test_full_moe64e_top4(cuda_device):
     assert rep["max_dlogp_mix"] <= tol and rep["max_dlogp1"] <= tol, rep
     # every token's first layers are compared before any divergence
     assert rep["decisions"] >= len(sample) * cfg.n_layers // 2
+
+
+def test_full_dense1b_ragged_paged_generation(cuda_device):
+    """The ragged headline variant in the bench's launch configuration (paged
+    cache of 64-position pages, batch 16, prompt lengths from the seeded
+    recipe, max_len = longest prompt + 128): every slot prefilled on its own,
+    then generation, each step fed the GPU's own draws.  The shortest and
+    the longest sequence are followed by the oracle, each alone, with the
+    same Philox noise at its own positions; a draw must equal the oracle's
+    unless its margin is within twice the measured log p_mix error (then it
+    must be a valid draw, and a sequence whose draw differs is followed no
+    further).  Tolerance as for dense1b_ctx1k (same model and depth)."""
+    import torch
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+    from oracle import Oracle
+    from oracle.sampling import gumbel, sample as oracle_sample
+    cfg = dfsynth.get_config("dense1b_ragged")
+    B, PG, steps, seed, span = cfg.batch, cfg.page_len, 3, 11, cfg.n_steps
+    lens = dfsynth.prompt_lengths(cfg, 0)
+    max_len = int(lens.max()) + span
+    n_pages = int(sum((int(n) + span + PG - 1) // PG for n in lens))
+    sample = [int(np.argmin(lens)), int(np.argmax(lens))]
+    w = _weights(cfg)
+    tok = dfsynth.tokens(cfg.with_(n_steps=span), 0)
+    m = DualFlowModel(cfg, w, max_batch=B, max_len=max_len, page_len=PG, n_pages=n_pages)
+    m.set_batch(B)
+    tok_d = torch.from_numpy(tok).cuda()
+    for b in range(B):
+        m.prefill_seq(b, tok_d[b, :int(lens[b])].contiguous())
+    x = torch.tensor([int(tok[b, lens[b]]) for b in range(B)], dtype=torch.int32, device="cuda")
+    out = torch.zeros(1, B, dtype=torch.int32, device="cuda")
+    lp = torch.zeros(B, cfg.vocab, device="cuda")
+    draws, lps = [], []
+    for s in range(steps):
+        m.generate(x, 1, seed, out, lp)
+        m.sync()
+        draws.append(out[0].cpu().numpy().astype(np.int64))
+        lps.append(lp.double().cpu().numpy())
+        x = out[0].clone()
+    assert m.seq_lengths()[:B] == [int(n) + steps for n in lens]
+    m.close()
+    tol, spread = spread_tolerance("dense1b_ctx1k", 2e-2)
+    compared = 0
+    for b in sample:
+        n = int(lens[b])
+        o = Oracle(cfg, w, 1, max_len=max_len)
+        o.prefill(tok[b:b + 1, :n])
+        t_in = int(tok[b, n])
+        for s in range(steps):
+            lo = o.decode_step(np.array([t_in]))["logp_mix"][0]
+            eps = float(np.abs(lps[s][b] - lo).max())
+            assert eps <= tol, (b, s, eps, tol)
+            x_o, margin = oracle_sample(lo, seed, n + s, b)
+            compared += 1
+            print("seq", b, "len", n, "step", s, "eps", eps, "margin", margin, "gpu", draws[s][b], "oracle", x_o)
+            if margin > 2 * eps:
+                assert draws[s][b] == x_o, (b, s)
+            else:
+                z = lo + gumbel(seed, n + s, b, cfg.vocab)
+                assert z.max() - z[draws[s][b]] <= 2 * eps, (b, s)
+                if draws[s][b] != x_o:
+                    break
+            t_in = int(draws[s][b])
+    assert compared >= 2
