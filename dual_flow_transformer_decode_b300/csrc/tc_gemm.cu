@@ -211,14 +211,17 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
         break;
       }
       case (int)TcOp::RESID: {
-        if (g0 < ep.n_out) {
-          if (prim) ep.h[(size_t)b * ep.d + g0] += v1.lo;
-          if (aux) ep.h[(size_t)(B + b) * ep.d + g0] += v2.lo;
-        }
-        if (g1 < ep.n_out) {
-          if (prim) ep.h[(size_t)b * ep.d + g1] += v1.hi;
-          if (aux) ep.h[(size_t)(B + b) * ep.d + g1] += v2.hi;
-        }
+        // every residual value this unit updates is loaded before any store,
+        // so the loads overlap instead of waiting on each other's stores
+        float* h1 = ep.h + (size_t)b * ep.d;
+        float* h2 = ep.h + (size_t)(B + b) * ep.d;
+        const bool k0 = g0 < ep.n_out, k1 = g1 < ep.n_out;
+        const float a0 = (prim && k0) ? h1[g0] : 0.f, a1 = (prim && k1) ? h1[g1] : 0.f;
+        const float c0 = (aux && k0) ? h2[g0] : 0.f, c1 = (aux && k1) ? h2[g1] : 0.f;
+        if (prim && k0) h1[g0] = a0 + v1.lo;
+        if (prim && k1) h1[g1] = a1 + v1.hi;
+        if (aux && k0) h2[g0] = c0 + v2.lo;
+        if (aux && k1) h2[g1] = c1 + v2.hi;
         break;
       }
       case (int)TcOp::SWIGLU: {
@@ -236,19 +239,26 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
         break;
       }
       case (int)TcOp::DOWN: {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int gn = k ? g1 : g0;
-          if (gn >= ep.n_out) continue;
-          const float y1 = k ? v1.hi : v1.lo;
-          if (prim) {
-            if (ep.C.save) ep.C.y1s[(size_t)b * ep.d + gn] = y1;
-            ep.h[(size_t)b * ep.d + gn] += y1;
+        // loads first (residual values, saved primary outputs), then stores
+        float* h1 = ep.h + (size_t)b * ep.d;
+        float* h2 = ep.h + (size_t)(B + b) * ep.d;
+        const float* ys = ep.C.y1s + (size_t)b * ep.d;
+        const bool k0 = g0 < ep.n_out, k1 = g1 < ep.n_out;
+        const float a0 = (prim && k0) ? h1[g0] : 0.f, a1 = (prim && k1) ? h1[g1] : 0.f;
+        const float c0 = (aux && k0) ? h2[g0] : 0.f, c1 = (aux && k1) ? h2[g1] : 0.f;
+        const bool sv = aux && ep.C.saved;
+        const float yp0 = (sv && k0) ? ys[g0] : v1.lo, yp1 = (sv && k1) ? ys[g1] : v1.hi;
+        if (prim) {
+          if (ep.C.save) {
+            if (k0) ep.C.y1s[(size_t)b * ep.d + g0] = v1.lo;
+            if (k1) ep.C.y1s[(size_t)b * ep.d + g1] = v1.hi;
           }
-          if (aux) {
-            const float yp = ep.C.saved ? ep.C.y1s[(size_t)b * ep.d + gn] : y1;
-            ep.h[(size_t)(B + b) * ep.d + gn] += fmaf(k ? cy : cx, yp, k ? v2.hi : v2.lo);
-          }
+          if (k0) h1[g0] = a0 + v1.lo;
+          if (k1) h1[g1] = a1 + v1.hi;
+        }
+        if (aux) {
+          if (k0) h2[g0] = c0 + fmaf(cx, yp0, v2.lo);
+          if (k1) h2[g1] = c1 + fmaf(cy, yp1, v2.hi);
         }
         break;
       }
