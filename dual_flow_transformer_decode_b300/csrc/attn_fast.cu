@@ -29,6 +29,8 @@
 
 #include <cooperative_groups.h>
 #include <math.h>
+
+#include <cmath>
 #include <stdlib.h>
 
 #include "attn_fast.h"
@@ -47,6 +49,7 @@ constexpr int BOX = TP * 64 * 2;  // one TMA box: 64 positions x 64 dims bf16 = 
 constexpr int STAGE = 4 * BOX;    // K lo, K hi, V lo, V hi = 32 KB
 constexpr int RQ = 16;            // query rows per MMA (m16)
 constexpr int kMaxSplits = 16;    // cluster size limit
+constexpr int kLaunchStages = 2;  // ring stages of a launch
 constexpr float kScale = 0.08838834764831845f;  // 1/sqrt(128)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -469,8 +472,53 @@ bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err) {
   }
   cudaFuncSetAttribute(k_attn_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(NSMAX));
   cudaFuncSetAttribute(k_attn_tma, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  // How many clusters of each size fit on the device at once.  A cluster's
+  // CTAs must share one GPC, so large clusters fit fewer times than the
+  // per-SM occupancy alone suggests.
+  for (int sp = 1; sp <= kMaxSplits; ++sp) {
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(sp, 1, 1);
+    lc.blockDim = dim3(160);
+    lc.dynamicSmemBytes = smem_bytes(kLaunchStages);
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = sp;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)k_attn_tma, &lc) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    P.max_clusters[sp] = n;
+  }
   P.enabled = true;
   return true;
+}
+
+int attn_fast_splits(const AttnPlan& P, const Dims& D, int B) {
+  const int pairs = B * D.Hkv;
+  const int T = (D.max_len + 63) / 64;
+  const double c0 = 4.0, c_tile = 1.5;  // as in attn_splits
+  int best = 1;
+  double best_t = 1e30;
+  for (int sp = 1; sp <= kMaxSplits && sp <= T; ++sp) {
+    // two clusters of headroom: the CTAs of the neighbouring kernels that
+    // programmatic dependent launch keeps resident displace some (measured at
+    // 16 pairs: 13-CTA clusters, 17 held on an idle device, ran 8% slower
+    // than 12-CTA clusters, 21 held)
+    const int cap = (P.max_clusters[sp] > 0 ? P.max_clusters[sp] : (2 * D.sms) / sp) - 2;
+    if (cap <= 0) break;
+    const double waves = std::ceil((double)pairs / cap);
+    const double tm = waves * (c0 + std::ceil((double)T / sp) * c_tile);
+    if (tm < best_t - 1e-9) {
+      best_t = tm;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 void attn_fast_free(AttnPlan& P) { P.enabled = false; }
@@ -489,7 +537,7 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   // Two ring stages: deeper rings or L2 prefetch of the split measured no
   // faster, and two stages let two attention CTAs share an SM with a CTA of
   // the next GEMM.
-  const int ns = 2, l2pf = 0;
+  const int ns = kLaunchStages, l2pf = 0;
   lc.dynamicSmemBytes = smem_bytes(ns);
   lc.stream = s;
   cudaLaunchAttribute at[2];

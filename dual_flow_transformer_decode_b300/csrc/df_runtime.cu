@@ -76,6 +76,7 @@ struct df_ctx {
   cudaStream_t stream = nullptr;
   bool own_stream = false;
   int B = 0, t = 0, splits = 1;
+  int splits_fast = 1;  // KV splits of the TMA attention kernel (cluster-capacity aware)
   bool ready = false;
   int aux_on = 1, ungrouped = 0;
   float *dbg_logp1 = nullptr, *dbg_logp2 = nullptr, *dbg_router = nullptr;
@@ -308,7 +309,7 @@ void op_qkv(df_ctx* X, int l, const Rows& R, const Couple& C) {
 void op_attn(df_ctx* X, int l, const Rows& R) {
   const Dims& D = X->D;
   if (!X->force_generic && df::attn_fast_can_run(X->at, D)) {
-    df::attn_fast(X->at, D, X->Bf, X->kv, l, X->splits, R, X->stream);  // merges its splits itself
+    df::attn_fast(X->at, D, X->Bf, X->kv, l, X->splits_fast, R, X->stream);  // merges its splits itself
   } else {
     df::launch_attention_generic(D, X->Bf, X->kv, l, X->splits, R, X->stream);
     df::launch_attn_combine(D, X->Bf, X->splits, R, X->stream);
@@ -748,6 +749,14 @@ static df_status set_batch(df_ctx* X, int B) {
     X->gen.reset();
     X->B = B;
     X->splits = df::attn_splits(X->D, B);
+    X->splits_fast = X->at.enabled ? df::attn_fast_splits(X->at, X->D, B) : X->splits;
+    const char* pp = getenv("DF_PRINT_PLAN");
+    if (pp && pp[0] == '1') {
+      fprintf(stderr, "df plan: B=%d attention splits %d (CUDA-core path %d); clusters held at once by size:", B,
+              X->splits_fast, X->splits);
+      for (int sp = 1; sp <= 16; ++sp) fprintf(stderr, " %d:%d", sp, X->at.max_clusters[sp]);
+      fprintf(stderr, "\n");
+    }
     std::string perr;
     if (!df::tc_plan_batch(X->tc, X->D, B, &perr)) return fail(X, DF_ERR_CUDA, perr);
     if (!df::mk_batch(X->mk, X->D, X->Bf, B, &perr)) return fail(X, DF_ERR_CUDA, perr);
