@@ -260,8 +260,9 @@ def run_ours(args, rank, world, local_rank):
                    "achieved_tflops": round(flop / (pms / 1e3) / 1e12, 1),
                    "peak_tflops": bf16_peak, "peak_kind": "measured bf16 sustained",
                    "frac_of_bf16_peak": round(flop / (pms / 1e3) / 1e12 / bf16_peak, 4),
-                   "path": "serial" if os.environ.get("DF_SERIAL_PREFILL") == "1" or cfg.n_experts or
-                   cfg.dtype != "bf16" else "batched"}
+                   "path": "serial" if os.environ.get("DF_SERIAL_PREFILL") == "1" or cfg.dtype != "bf16" or
+                   cfg.head_dim != 128 or (cfg.n_experts and (cfg.n_experts > 1024 or cfg.top_k > 16 or
+                                                             cfg.expert_hidden % 64)) else "batched"}
     model.sync()
     # [span][B]: step s feeds sequence b its token at position lens[b] + s
     steps_idx = torch.from_numpy(lens[None, :] + np.arange(span)[:, None]).to(dev)

@@ -141,7 +141,10 @@ void launch_embed(const Dims& D, const Buffers& Bf, const void* emb1, const void
 void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out, float* out_f32,
                     const Rows& R, cudaStream_t s);
 // RMSNorm of rows 0..rows-1 of h (row stride d) into out (storage type).
-void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s);
+void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s,
+                         float* out_f32 = nullptr);
+// Router logits rlog[m][E] of rows 0..rows-1 of an unrounded normed buffer.
+void launch_router_rows(const Dims& D, const void* Wr, const float* un, float* rlog, int rows, cudaStream_t s);
 
 // CUDA-core GEMV: out[m][n] = sum_k W[n][k] X[m][k] for rows m in [lo, hi).
 // x_f32: X is fp32 (router) instead of dtype.

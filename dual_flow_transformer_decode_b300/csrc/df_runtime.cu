@@ -580,10 +580,10 @@ df_status run_captured(df_ctx* X, GraphSlot& slot, const GraphKey& key, F&& enqu
 // Prefill of n positions: all B sequences (nseq = B, slot0 = 0) or one slot
 // (nseq = 1).  Positions must start at 0 (set by the caller).
 df_status prefill_rows(df_ctx* X, const int32_t* tokens, int nseq, int n, int slot0, int B) {
-  if (X->bp.enabled && X->tc.enabled && X->at.enabled && !X->force_generic) {
+  if (X->bp.enabled && X->tc.enabled && X->at.enabled && (!X->D.E || X->moe.enabled) && !X->force_generic) {
     // batched: every layer once per chunk of positions (kernels enqueued directly)
-    df::bp_prefill(X->bp, X->tc, X->at, X->D, X->Bf, X->kv, X->emb1, X->attn_norm.data(), X->mlp_norm.data(),
-                   tokens, nseq, n, slot0, X->stream);
+    df::bp_prefill(X->bp, X->tc, X->at, &X->moe, X->D, X->Bf, X->kv, X->emb1, X->attn_norm.data(),
+                   X->mlp_norm.data(), X->router.data(), tokens, nseq, n, slot0, X->stream);
     df::launch_set_pos(X->Bf.ctrl, n, X->stream);
     if (X->D.paged) {
       EditQueue pq{X, X->Bf.kv_pos};

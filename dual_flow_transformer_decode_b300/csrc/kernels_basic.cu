@@ -192,13 +192,14 @@ void launch_rmsnorm(const Dims& D, const Buffers& Bf, const float* g, void* out,
     launch_pdl(k_rmsnorm<float>, dim3(n), dim3(256), 0, s, Bf.h, g, (float*)out, out_f32, D.d, D.eps, R.lo);
 }
 
-void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s) {
+void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* out, int rows, cudaStream_t s,
+                         float* out_f32) {
   if (rows <= 0) return;
   if (D.bf16)
-    launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, h, g, (__nv_bfloat16*)out, (float*)nullptr,
-               D.d, D.eps, 0);
+    launch_pdl(k_rmsnorm<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, h, g, (__nv_bfloat16*)out, out_f32, D.d, D.eps,
+               0);
   else
-    launch_pdl(k_rmsnorm<float>, dim3(rows), dim3(256), 0, s, h, g, (float*)out, (float*)nullptr, D.d, D.eps, 0);
+    launch_pdl(k_rmsnorm<float>, dim3(rows), dim3(256), 0, s, h, g, (float*)out, out_f32, D.d, D.eps, 0);
 }
 
 // ------------------------------------------------------------------ GEMV (CUDA cores)
@@ -873,6 +874,17 @@ void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows&
   else
     launch_pdl(k_router<float, kRouterRows>, grid, dim3(256), smem, s, (const float*)Wr, (const float*)Bf.un,
                Bf.rlog, D.E, D.d, R.lo, R.hi);
+}
+
+void launch_router_rows(const Dims& D, const void* Wr, const float* un, float* rlog, int rows, cudaStream_t s) {
+  if (rows <= 0) return;
+  const dim3 grid((rows + kRouterRows - 1) / kRouterRows, (D.E + 7) / 8);
+  const size_t smem = (size_t)kRouterRows * D.d * sizeof(float);
+  if (D.bf16)
+    launch_pdl(k_router<__nv_bfloat16, kRouterRows>, grid, dim3(256), smem, s, (const __nv_bfloat16*)Wr, un, rlog,
+               D.E, D.d, 0, rows);
+  else
+    launch_pdl(k_router<float, kRouterRows>, grid, dim3(256), smem, s, (const float*)Wr, un, rlog, D.E, D.d, 0, rows);
 }
 
 // The primary rows choose their top-k experts (descending router logit,

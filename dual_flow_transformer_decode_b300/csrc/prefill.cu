@@ -40,6 +40,7 @@
 #include "prefill.h"
 #include "ptx.cuh"
 #include "tc_gemm.h"
+#include "tc_moe.h"
 
 namespace df {
 
@@ -55,7 +56,7 @@ constexpr int kStages = 6;
 constexpr int kChunkRows = 2048;
 constexpr int kHD = 128;
 
-enum : int { BP_QKV = 0, BP_RESID = 1, BP_SWIGLU = 2 };
+enum : int { BP_QKV = 0, BP_RESID = 1, BP_SWIGLU = 2, BP_YOUT = 3 };
 
 struct BpEp {
   int op;
@@ -72,6 +73,13 @@ struct BpEp {
   int d;
   __nv_bfloat16* z;     // SwiGLU output [rows][F]
   int F;
+  // Grouped expert GEMMs (MoE): row tile rt of the launch is entry rt of the
+  // block table gblk[rt] = (expert, first packed row), expert -1 meaning no
+  // block; the weights of expert e start at weight row e * wrows.
+  const int* gblk;
+  int wrows;
+  float* y;             // BP_YOUT: fp32 output rows [rows][ldy]
+  int ldy;
 };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -119,6 +127,17 @@ __global__ void __launch_bounds__(128, 1)
   volatile int* flags = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x, ft = blockIdx.y;
+  // activation rows and weight rows of this tile
+  int xrow0 = rt * kBM, wrow0 = ft * kBN;
+  if (ep.gblk) {
+    // the block table comes from the previous kernel; a tile past the table's
+    // end leaves before taking any resource
+    ptx::grid_dep_wait();
+    const int ex = ep.gblk[2 * rt];
+    if (ex < 0) return;  // uniform across the CTA
+    xrow0 = ep.gblk[2 * rt + 1];
+    wrow0 = ex * ep.wrows + ft * kBN;
+  }
   if (tid == 0) {
     ptx::prefetch_tmap(&tx);
     ptx::prefetch_tmap(&tw);
@@ -152,8 +171,8 @@ __global__ void __launch_bounds__(128, 1)
       }
       uint8_t* a = base + (size_t)s * kStage;
       ptx::mbar_arrive_expect_tx(&full[s], kStage);
-      ptx::tma_load_2d(a, &tx, &full[s], i * kBK, rt * kBM);
-      ptx::tma_load_2d(a + kStageA, &tw, &full[s], i * kBK, ft * kBN);
+      ptx::tma_load_2d(a, &tx, &full[s], i * kBK, xrow0);
+      ptx::tma_load_2d(a + kStageA, &tw, &full[s], i * kBK, wrow0);
       issued = i + 1;
     }
     if (flags[0]) {
@@ -191,11 +210,11 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   ptx::grid_dep_launch();
   if (!flags[0]) {
-    const int r = warp * 32 + lane, m = rt * kBM + r;
+    const int r = warp * 32 + lane, m = xrow0 + r;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     const int n0 = ft * kBN;
     const int b = m / ep.C, i = m % ep.C, pos = ep.p0 + i;
-    const bool valid = m < ep.Mc;
+    const bool valid = ep.gblk ? true : m < ep.Mc;  // packed expert blocks: padding rows are computed, never read
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float lo[16], hi[16];
@@ -236,6 +255,15 @@ __global__ void __launch_bounds__(128, 1)
         float* hr = ep.h + (size_t)m * ep.d + n0;
         add16(hr + 16 * c, lo);
         add16(hr + 64 + 16 * c, hi);
+      } else if (ep.op == BP_YOUT) {
+        float* yr = ep.y + (size_t)m * ep.ldy + n0;
+        float4* y4 = reinterpret_cast<float4*>(yr + 16 * c);
+        float4* y5 = reinterpret_cast<float4*>(yr + 64 + 16 * c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          y4[q] = make_float4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+          y5[q] = make_float4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        }
       } else {  // BP_SWIGLU: rows 0..63 of the tile are gate, 64..127 up, of z features 64 ft ..
         float zv[16];
 #pragma unroll
@@ -484,6 +512,147 @@ __global__ void __launch_bounds__(160, 1)
 
 size_t attn_smem() { return 1024 + (size_t)ANS * ASTAGE + 2 * ANS * 8 + 16; }
 
+// ------------------------------------------------------------------ MoE (router replay's primary routing)
+//
+// "Mecanismos Clave" (Replay de Router): prefill runs the primary flow, whose
+// router picks each token's top-k experts (descending router logit, ties to
+// the lower index) and gates them with the softmax of those logits.  The
+// chunk's rows are grouped by expert: each chosen (row, j) takes a slot in
+// its expert's list, the expert's rows are packed into 128-row blocks, the
+// expert GEMMs run over the blocks, and each row sums its k gated expert
+// outputs in j order.  A row's result does not depend on its slot, so the
+// order in which rows take slots does not change any value.
+
+constexpr int kRouteWarps = 8;
+constexpr int kMaxRouteK = 16;
+
+__global__ void __launch_bounds__(32 * kRouteWarps)
+    k_pf_route(const float* __restrict__ rlog, int Mc, int E, int k, int* __restrict__ ecount,
+               int* __restrict__ sel_e, int* __restrict__ sel_slot, float* __restrict__ sel_g) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  __shared__ int ch[kRouteWarps][kMaxRouteK];
+  __shared__ float cv[kRouteWarps][kMaxRouteK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x * kRouteWarps + warp;
+  if (m >= Mc) return;  // uniform across the warp
+  const float* r = rlog + (size_t)m * E;
+  uint32_t taken = 0;  // bit t: expert lane + 32 t already chosen (E <= 1024)
+  for (int j = 0; j < k; ++j) {
+    // a NaN logit counts as -inf, and ties go to the lower index, so one of
+    // the (at least E - j > 0) untaken experts is always chosen
+    float best = -INFINITY;
+    int bi = E;
+    for (int t = 0, e = lane; e < E; ++t, e += 32) {
+      if ((taken >> t) & 1u) continue;
+      float v = r[e];
+      if (!(v == v)) v = -INFINITY;
+      if (v > best || (v == best && e < bi)) {
+        best = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      ch[warp][j] = bi;
+      cv[warp][j] = best;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    // softmax over the chosen logits (the first is the largest)
+    float mx = -INFINITY;
+    for (int j = 0; j < k; ++j) mx = fmaxf(mx, cv[warp][j]);
+    float den = 0.f;
+    for (int j = 0; j < k; ++j) den += expf(cv[warp][j] - mx);
+    for (int j = 0; j < k; ++j) {
+      const int e = ch[warp][j];
+      sel_e[(size_t)m * k + j] = e;
+      sel_slot[(size_t)m * k + j] = atomicAdd(&ecount[e], 1);
+      sel_g[(size_t)m * k + j] = expf(cv[warp][j] - mx) / den;
+    }
+  }
+}
+
+// Packed layout: expert e's rows start at poff[e] (a multiple of 128); the
+// block table lists (expert, first row) for each 128-row block, then -1.
+__global__ void k_pf_blocks(const int* __restrict__ ecount, int E, int* __restrict__ poff, int* __restrict__ gblk,
+                            int maxblk) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  if (threadIdx.x != 0) return;
+  int nb = 0;
+  for (int e = 0; e < E; ++e) {
+    poff[e] = nb * kBM;
+    const int eb = (ecount[e] + kBM - 1) / kBM;
+    for (int i = 0; i < eb && nb < maxblk; ++i, ++nb) {
+      gblk[2 * nb] = e;
+      gblk[2 * nb + 1] = nb * kBM;
+    }
+  }
+  for (int i = nb; i < maxblk; ++i) gblk[2 * i] = -1;
+}
+
+// Entry (m, j) = row m's j-th expert: copy normed row m into the expert's
+// packed block (one warp per entry, 16-byte copies; d is a multiple of 8).
+__global__ void k_pf_gather(const __nv_bfloat16* __restrict__ u, const int* __restrict__ sel_e,
+                            const int* __restrict__ sel_slot, const int* __restrict__ poff, int nent, int k, int d,
+                            __nv_bfloat16* __restrict__ xg) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ent = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (ent >= nent) return;
+  const int m = ent / k;
+  const int row = poff[sel_e[ent]] + sel_slot[ent];
+  const uint4* src = reinterpret_cast<const uint4*>(u + (size_t)m * d);
+  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)row * d);
+  for (int i = lane; i < d / 8; i += 32) dst[i] = src[i];
+}
+
+// h[m] += sum_j g_j * y[packed row of (m, j)], j in order (fp32).
+__global__ void k_pf_combine(const float* __restrict__ yp, const int* __restrict__ sel_e,
+                             const int* __restrict__ sel_slot, const float* __restrict__ sel_g,
+                             const int* __restrict__ poff, int k, int d, float* __restrict__ h) {
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int m = blockIdx.x;
+  __shared__ int rows[kMaxRouteK];
+  __shared__ float gs[kMaxRouteK];
+  if (threadIdx.x < k) {
+    rows[threadIdx.x] = poff[sel_e[(size_t)m * k + threadIdx.x]] + sel_slot[(size_t)m * k + threadIdx.x];
+    gs[threadIdx.x] = sel_g[(size_t)m * k + threadIdx.x];
+  }
+  __syncthreads();
+  float4* hr = reinterpret_cast<float4*>(h + (size_t)m * d);
+  for (int c = threadIdx.x; c < d / 4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 y = reinterpret_cast<const float4*>(yp + (size_t)rows[j] * d)[c];
+      const float g = gs[j];
+      acc.x = fmaf(g, y.x, acc.x);
+      acc.y = fmaf(g, y.y, acc.y);
+      acc.z = fmaf(g, y.z, acc.z);
+      acc.w = fmaf(g, y.w, acc.w);
+    }
+    float4 x = hr[c];
+    x.x += acc.x;
+    x.y += acc.y;
+    x.z += acc.z;
+    x.w += acc.w;
+    hr[c] = x;
+  }
+}
+
 // ------------------------------------------------------------------ embedding
 
 // h[b*C + i] = E1[tokens[b][p0 + i]] for the chunk (primary flow only).
@@ -541,8 +710,8 @@ void launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 }
 
 void gemm(const CUtensorMap& tx, const CUtensorMap& tw, int K, int n_out, const BpEp& ep, Ctrl* ctrl,
-          cudaStream_t s) {
-  const dim3 grid((ep.Mc + kBM - 1) / kBM, n_out / kBN);
+          cudaStream_t s, int row_tiles = 0) {
+  const dim3 grid(row_tiles ? row_tiles : (ep.Mc + kBM - 1) / kBM, n_out / kBN);
   launch_ex(k_bp_gemm, grid, dim3(128), gemm_smem(), s, tx, tw, K / kBK, ep, ctrl);
 }
 
@@ -551,17 +720,28 @@ void gemm(const CUtensorMap& tx, const CUtensorMap& tw, int K, int n_out, const 
 int bp_rows(const Dims& D) {
   const char* e = getenv("DF_SERIAL_PREFILL");
   if (e && e[0] == '1') return 0;
-  if (!D.bf16 || D.E || D.hd != kHD) return 0;
+  if (!D.bf16 || D.hd != kHD) return 0;
   if (D.d % kBN || D.qdim % kBN || D.kvdim % kBN || D.F % 64 || D.d % kBK || D.qdim % kBK) return 0;
+  if (D.E && (D.Fe % 64 || D.E > 1024 || D.k > kMaxRouteK)) return 0;
   if (2 * D.G > 64) return 0;
   const int rows = std::max(kChunkRows, (D.maxB + kBM - 1) / kBM * kBM);
   return rows;
 }
 
+// 128-row blocks of the packed expert buffers for chunks of R rows: every
+// entry, plus a partial block per expert.
+int moe_blocks(const Dims& D, int R) { return (R * D.k + kBM - 1) / kBM + D.E; }
+
 size_t bp_workspace_bytes(const Dims& D) {
   const size_t R = (size_t)bp_rows(D);
   if (!R) return 0;
-  return R * D.d * 4 + R * D.d * 2 + 2 * R * D.qdim * 2 + R * (size_t)D.F * 2 + 4 * 256;
+  size_t b = R * D.d * 4 + R * D.d * 2 + 2 * R * D.qdim * 2 + R * (size_t)D.F * 2 + 5 * 256;
+  if (D.E) {
+    const size_t rows = (size_t)moe_blocks(D, (int)R) * kBM;
+    b += R * D.d * 4 + R * D.E * 4 + 3 * R * D.k * 4 + 2 * (size_t)D.E * 4 + (size_t)moe_blocks(D, (int)R) * 8 +
+         rows * D.d * 2 + rows * D.Fe * 2 + rows * D.d * 4 + 12 * 256;
+  }
+  return b;
 }
 
 bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err) {
@@ -579,8 +759,26 @@ bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err) {
   P.u = take((size_t)R * D.d * 2);
   P.q = take((size_t)R * D.qdim * 2);
   P.o = take((size_t)R * D.qdim * 2);
-  P.z = take((size_t)R * D.F * 2);
-  bool ok = map_rows(&P.x_u, P.u, D.d, R) && map_rows(&P.x_o, P.o, D.qdim, R) && map_rows(&P.x_z, P.z, D.F, R);
+  P.z = take((size_t)R * (D.F ? D.F : 64) * 2);
+  bool ok = map_rows(&P.x_u, P.u, D.d, R) && map_rows(&P.x_o, P.o, D.qdim, R);
+  if (D.F) ok = ok && map_rows(&P.x_z, P.z, D.F, R);
+  if (D.E) {
+    P.moe = true;
+    P.maxblk = moe_blocks(D, R);
+    const size_t rows = (size_t)P.maxblk * kBM;
+    P.un = reinterpret_cast<float*>(take((size_t)R * D.d * 4));
+    P.rlog = reinterpret_cast<float*>(take((size_t)R * D.E * 4));
+    P.sel_e = reinterpret_cast<int*>(take((size_t)R * D.k * 4));
+    P.sel_slot = reinterpret_cast<int*>(take((size_t)R * D.k * 4));
+    P.sel_g = reinterpret_cast<float*>(take((size_t)R * D.k * 4));
+    P.ecount = reinterpret_cast<int*>(take((size_t)D.E * 4));
+    P.poff = reinterpret_cast<int*>(take((size_t)D.E * 4));
+    P.gblk = reinterpret_cast<int*>(take((size_t)P.maxblk * 8));
+    P.xg = take(rows * D.d * 2);
+    P.zg = take(rows * D.Fe * 2);
+    P.yg = reinterpret_cast<float*>(take(rows * D.d * 4));
+    ok = ok && map_rows(&P.x_xg, P.xg, D.d, rows) && map_rows(&P.x_zg, P.zg, D.Fe, rows);
+  }
   if (!ok) {
     if (err) *err = "cuTensorMapEncodeTiled failed (prefill activation maps)";
     return false;
@@ -595,9 +793,10 @@ bool bp_init(BpPlan& P, const Dims& D, void* region, std::string* err) {
   return true;
 }
 
-void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dims& D, const Buffers& Bf,
-                void* kv, const void* emb1, const float* const* attn_norm, const float* const* mlp_norm,
-                const int32_t* tokens, int B, int n, int slot0, cudaStream_t s) {
+void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const MoePlan* moe, const Dims& D,
+                const Buffers& Bf, void* kv, const void* emb1, const float* const* attn_norm,
+                const float* const* mlp_norm, const void* const* router, const int32_t* tokens, int B, int n,
+                int slot0, cudaStream_t s) {
   const int C = std::max(1, P.mcap / B);
   __nv_bfloat16* kvb = static_cast<__nv_bfloat16*>(kv);
   for (int p0 = 0; p0 < n; p0 += C) {
@@ -630,11 +829,40 @@ void bp_prefill(const BpPlan& P, const TcPlan& tc, const AttnPlan& at, const Dim
                 D.Hkv, D.G, D.qdim, Ce, p0);
       ep.op = BP_RESID;
       gemm(P.x_o, tc.w_o[l], D.qdim, D.d, ep, Bf.ctrl, s);
-      launch_rmsnorm_rows(D, P.h, mlp_norm[l], P.u, Mc, s);
-      ep.op = BP_SWIGLU;
-      gemm(P.x_u, tc.w_gu[l], D.d, 2 * D.F, ep, Bf.ctrl, s);
-      ep.op = BP_RESID;
-      gemm(P.x_z, tc.w_d[l], D.F, D.d, ep, Bf.ctrl, s);
+      if (!D.E) {
+        launch_rmsnorm_rows(D, P.h, mlp_norm[l], P.u, Mc, s);
+        ep.op = BP_SWIGLU;
+        gemm(P.x_u, tc.w_gu[l], D.d, 2 * D.F, ep, Bf.ctrl, s);
+        ep.op = BP_RESID;
+        gemm(P.x_z, tc.w_d[l], D.F, D.d, ep, Bf.ctrl, s);
+        continue;
+      }
+      // MoE layer: route the chunk's rows, run the experts over their packed
+      // blocks, add each row's gated expert outputs to its residual
+      launch_rmsnorm_rows(D, P.h, mlp_norm[l], P.u, Mc, s, P.un);
+      launch_router_rows(D, router[l], P.un, P.rlog, Mc, s);
+      cudaMemsetAsync(P.ecount, 0, (size_t)D.E * 4, s);
+      launch_ex(k_pf_route, dim3((Mc + kRouteWarps - 1) / kRouteWarps), dim3(32 * kRouteWarps), 0, s,
+                (const float*)P.rlog, Mc, D.E, D.k, P.ecount, P.sel_e, P.sel_slot, P.sel_g);
+      launch_ex(k_pf_blocks, dim3(1), dim3(32), 0, s, (const int*)P.ecount, D.E, P.poff, P.gblk, P.maxblk);
+      const int nent = Mc * D.k;
+      launch_ex(k_pf_gather, dim3((nent + 7) / 8), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(P.u),
+                (const int*)P.sel_e, (const int*)P.sel_slot, (const int*)P.poff, nent, D.k, D.d,
+                static_cast<__nv_bfloat16*>(P.xg));
+      BpEp eg = ep;
+      eg.gblk = P.gblk;
+      eg.op = BP_SWIGLU;
+      eg.z = static_cast<__nv_bfloat16*>(P.zg);
+      eg.F = D.Fe;
+      eg.wrows = 2 * D.Fe;
+      gemm(P.x_xg, moe->w_gu[l], D.d, 2 * D.Fe, eg, Bf.ctrl, s, P.maxblk);
+      eg.op = BP_YOUT;
+      eg.y = P.yg;
+      eg.ldy = D.d;
+      eg.wrows = D.d;
+      gemm(P.x_zg, moe->w_d[l], D.Fe, D.d, eg, Bf.ctrl, s, P.maxblk);
+      launch_ex(k_pf_combine, dim3(Mc), dim3(256), 0, s, (const float*)P.yg, (const int*)P.sel_e,
+                (const int*)P.sel_slot, (const float*)P.sel_g, (const int*)P.poff, D.k, D.d, P.h);
     }
   }
 }

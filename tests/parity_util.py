@@ -284,6 +284,25 @@ def compare_moe_steps(cfg, gpu_steps, ora_steps, seq_map):
                     if set(gs) != set(os_):
                         diverged[i] = True
                         rep["diverged_at"].append((s, l, i))
+                if not diverged[i] and "topk_aux" in g and "topk_aux" in o:
+                    # the auxiliary flow's own experts, ranked by its router
+                    # logits (not exported; their deviation bounded by twice
+                    # the primary row's); a valid near tie taken the other way
+                    # changes the auxiliary computation from here on
+                    eps2 = 2 * eps
+                    rep["decisions"] += 1
+                    gx, ox = list(g["topk_aux"][l, b]), list(o["topk_aux"][l][i])
+                    if o["topk_aux_margin"][l, i] > 2 * eps2:
+                        if set(gx) != set(ox):
+                            rep["topk_mismatch"].append(("aux", s, l, i, gx, ox, float(o["topk_aux_margin"][l, i]), eps2))
+                    else:
+                        rep["near_ties"].append(("topk_aux", s, l, i, float(o["topk_aux_margin"][l, i]), eps2))
+                        r2 = o["router2"][l][i]
+                        if r2[ox].min() - r2[gx].min() > 2 * eps2:
+                            rep["invalid_near_ties"].append(("topk_aux", s, l, i, gx, ox))
+                        if set(gx) != set(ox):
+                            diverged[i] = True
+                            rep["diverged_at"].append((s, l, i))
             if diverged[i]:
                 rep["pairs_diverged"] += 1
                 continue

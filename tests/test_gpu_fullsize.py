@@ -102,13 +102,15 @@ def test_full_synthetic_context(name, sample, steps, cuda_device):
     assert mx <= kmax and rel <= krel
 
 
-def test_full_moe64e_top4(cuda_device):
-    """MoE with router replay at full size.  Router-logit deviations of the
-    size of the bf16 cascade put some top-k decisions inside the near-tie
-    band; a token whose routing takes the other valid branch follows another
-    computation from there on, so values are compared until then (see
-    parity_util.compare_moe_steps)."""
-    name, sample, steps = "moe64e_top4", [0, 31], 3
+@pytest.mark.parametrize("name", ["moe64e_top4", "moe64e_top4_aux8"])
+def test_full_moe64e_top4(name, cuda_device):
+    """MoE with router replay at full size, and the variant whose auxiliary
+    flow adds 4 experts of its own (the same model; tolerance from its
+    spread).  Router-logit deviations of the size of the bf16 cascade put
+    some top-k decisions inside the near-tie band; a token whose routing
+    takes the other valid branch follows another computation from there on,
+    so values are compared until then (see parity_util.compare_moe_steps)."""
+    sample, steps = [0, 31], 3
     cfg = dfsynth.get_config(name)
     w = Weights(cfg, 0)
     w.prefetch()
@@ -117,7 +119,7 @@ def test_full_moe64e_top4(cuda_device):
     g.close()
     o, outs = oracle_run_synthetic(cfg, w, tok, sample, steps)
     rep = compare_moe_steps(cfg, g.steps, outs, sample)
-    tol, spread = spread_tolerance(cfg.name, 2e-2)
+    tol, spread = spread_tolerance("moe64e_top4", 2e-2)
     print({k: v for k, v in rep.items() if not isinstance(v, list) or k == "diverged_at"}, "tol", tol)
     assert not rep["self_inconsistent"], rep["self_inconsistent"][:5]
     assert not rep["topk_mismatch"], rep["topk_mismatch"][:5]

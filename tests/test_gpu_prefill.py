@@ -1,5 +1,7 @@
 """Batched (chunked) prefill against the token-serial prefill of the same
 library, and against the oracle through the decode steps that follow.
+MoE models route the chunk's rows, pack each expert's rows into 128-row
+blocks and run the experts as grouped GEMMs.
 
 The batched path runs every layer once per chunk of positions with tensor-core
 GEMMs over B x C rows and a causal attention kernel over the cache; the
@@ -35,6 +37,8 @@ def _serial(cfg, w, tok, **kw):
     ("t_bf16_long", 1100, None),  # batch 2: two chunks, attention across the chunk boundary
     ("t_bf16", 1, None),          # a single position
     ("t_bf16", 65, 1),            # batch 1, one position past a tile
+    ("t_moe", 33, None),          # MoE: routed rows packed per expert
+    ("t_moe", 300, None),         # MoE: several 128-row blocks per expert
 ])
 def test_batched_prefill_matches_serial(name, n_prefill, batch, cuda_device):
     cfg = dfsynth.get_config(name).with_(n_prefill=n_prefill, n_steps=3)
