@@ -57,3 +57,45 @@ def test_invalid_configs_rejected(lib):
         c = binding.make_config(cfg, 1, 16)
         setattr(c, field, val)
         assert binding.df_workspace_bytes(c)[0] == 0, field
+
+
+@pytest.mark.parametrize("page_len,n_pages", [(64, 40), (128, 7), (1024, 3)])
+def test_paged_cache_size(lib, page_len, n_pages):
+    """Paged cache: n_pages + 1 pages (the last a sink for free slots) of
+    page_len positions for every layer, K and V, and KV head."""
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config("dense1b_ctx1k")
+    ws, kv = binding.df_workspace_bytes(binding.make_config(cfg, cfg.batch, cfg.max_len, page_len, n_pages))
+    assert ws > 0
+    assert kv == cfg.n_layers * 2 * (n_pages + 1) * cfg.n_kv_heads * page_len * cfg.head_dim * 2
+    # the persistent single-launch pass (contiguous caches only) reserves no
+    # region here, so the paged workspace is the smaller one
+    ws0, _ = binding.df_workspace_bytes(binding.make_config(cfg, cfg.batch, cfg.max_len))
+    assert 0 < ws < ws0
+
+
+def test_invalid_paged_configs_rejected(lib):
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config("t_bf16")
+    assert binding.df_workspace_bytes(binding.make_config(cfg, 3, 160, 64, 9))[0] > 0
+    for page_len, n_pages in [(32, 9), (96, 9), (64, 0), (0, 9), (1 << 21, 1)]:
+        c = binding.make_config(cfg, 3, 160, page_len, n_pages)
+        assert binding.df_workspace_bytes(c)[0] == 0, (page_len, n_pages)
+
+
+def test_aux_top_k_range(lib):
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config("t_moe")
+    for aux, ok in [(0, True), (2, True), (4, True), (8, True), (1, False), (9, False)]:
+        c = binding.make_config(cfg.with_(aux_top_k=aux), 5, 40)
+        assert (binding.df_workspace_bytes(c)[0] > 0) == ok, aux
+
+
+def test_moe_batched_prefill_workspace(lib):
+    """MoE models reserve the batched-prefill buffers (routed rows packed per
+    expert): the workspace grows with the expert count and width."""
+    from dual_flow_transformer_decode_b300 import binding
+    cfg = dfsynth.get_config("t_moe")
+    small, _ = binding.df_workspace_bytes(binding.make_config(cfg, 5, 40))
+    big, _ = binding.df_workspace_bytes(binding.make_config(cfg.with_(expert_hidden=384), 5, 40))
+    assert big > small > 0
