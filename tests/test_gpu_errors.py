@@ -75,3 +75,64 @@ def test_empty_prompt_then_decode(cuda_device):
     assert m.length == 1
     assert abs(float(lp.exp().sum()) - 1.0) < 1e-4
     m.close()
+
+
+def test_slot_calls_need_a_paged_cache(cuda_device):
+    import torch
+    from dual_flow_transformer_decode_b300 import binding as b
+    cfg = dfsynth.get_config("t_bf16")
+    m = _model(cfg)
+    m.prefill(torch.zeros(cfg.batch, 5, dtype=torch.int32, device="cuda"))
+    for call in (lambda: m.set_batch(2), lambda: m.release_seq(0),
+                 lambda: m.prefill_seq(0, torch.zeros(3, dtype=torch.int32, device="cuda"))):
+        with pytest.raises(b.DFError) as e:
+            call()
+        assert e.value.status == b.DF_ERR_UNSUPPORTED
+    with pytest.raises(b.DFError):
+        m.seq_pages(0)
+    assert m.seq_lengths()[:cfg.batch] == [5] * cfg.batch
+    m.sync()
+    m.close()
+
+
+def test_paged_and_generation_argument_errors(cuda_device):
+    """Every refusal comes back before anything is enqueued: the lengths and
+    the page pool are unchanged and the next valid call works."""
+    import torch
+    from dual_flow_transformer_decode_b300 import binding as b
+    cfg = dfsynth.get_config("t_bf16")
+    m = _model(cfg, max_batch=3, max_len=100, page_len=64, n_pages=4)
+    tok = torch.zeros(40, dtype=torch.int32, device="cuda")
+    with pytest.raises(b.DFError) as e:
+        m.prefill_seq(0, tok)          # before any batch size is set
+    assert e.value.status == b.DF_ERR_STATE
+    m.set_batch(2)
+    with pytest.raises(b.DFError) as e:
+        m.prefill_seq(2, tok)          # slot beyond the batch
+    assert e.value.status == b.DF_ERR_ARG
+    with pytest.raises(b.DFError) as e:
+        m.prefill_seq(0, torch.zeros(101, dtype=torch.int32, device="cuda"))
+    assert e.value.status == b.DF_ERR_CAPACITY
+    with pytest.raises(b.DFError) as e:
+        m.set_batch(4)                 # more slots than max_batch
+    assert e.value.status == b.DF_ERR_ARG
+    m.prefill_seq(0, tok)
+    m.release_seq(1)                   # releasing a free slot is a no-op
+    assert m.seq_lengths()[:2] == [40, -1]
+    x = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.zeros(4, 2, dtype=torch.int32, device="cuda")
+    with pytest.raises(b.DFError) as e:
+        m.generate(x, -1, 0, out)
+    assert e.value.status == b.DF_ERR_ARG
+    with pytest.raises(b.DFError) as e:
+        m.generate(x, 61, 0, torch.zeros(61, 2, dtype=torch.int32, device="cuda"))  # 40 + 61 > 100
+    assert e.value.status == b.DF_ERR_CAPACITY
+    assert m.seq_lengths()[:2] == [40, -1]
+    with pytest.raises(b.DFError) as e:
+        b.df_generate(m.ctx, x.data_ptr(), 2, 0, 0)   # no output buffer
+    assert e.value.status == b.DF_ERR_ARG
+    m.generate(x, 4, 0, out)
+    m.sync()
+    assert m.seq_lengths()[:2] == [44, -1]
+    assert int(out[:, 0].min()) >= 0 and int(out[:, 0].max()) < cfg.vocab
+    m.close()
