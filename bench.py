@@ -140,6 +140,23 @@ def captured_traffic(workload: str, op: str):
     return None
 
 
+def dist_max(x: float, dist_mod=None, device="cpu") -> float:
+    """A per-rank value's maximum over all ranks (a job's time is its slowest
+    rank's); the identity on a single process."""
+    if dist_mod is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, B: int, K: int, ms_total: float) -> float:
+    """Whole-job throughput: each of `world` replicas decodes B sequences for
+    K steps (weak scaling), timed by the slowest rank."""
+    return world * B * K / (ms_total / 1e3)
+
+
 def algorithmic_bytes(cfg, op: str, B: int, t: int, moe_union: float | None = None) -> float:
     """Bytes one launch of an operation must move: weights read once, KV read
     once, KV appended, logits written."""
@@ -300,11 +317,7 @@ def run_ours(args, rank, world, local_rank):
         return e0.elapsed_time(e1)
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return dist_max(x, dist, dev)
 
     # main measurement: grouped step
     clocks = Clocks(local_rank)
@@ -314,7 +327,7 @@ def run_ours(args, rank, world, local_rank):
     ms_total = max_over_ranks(ms_total)
     kernels = model.step_kernels
     ms_step = ms_total / K
-    tokens_s = world * B * K / (ms_total / 1e3)
+    tokens_s = job_tokens_per_s(world, B, K, ms_total)
     t_mid = P + W + K // 2           # mean position of the timed steps (ragged: offset from the mean prompt)
     t_mean = int(round(P_mean)) + W + K // 2
     if args.quick:
