@@ -835,7 +835,26 @@ __global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const
   extern __shared__ float xrows[];  // [R][d]
   const int m0 = lo + blockIdx.x * R;
   const int nr = min(R, hi - m0);
-  for (int i = threadIdx.x; i < nr * d; i += blockDim.x) xrows[i] = un[(size_t)m0 * d + i];
+  {
+    // 16-byte copies, a batch of loads in flight before the stores (d is a
+    // multiple of 8)
+    const float4* src = reinterpret_cast<const float4*>(un + (size_t)m0 * d);
+    float4* dst = reinterpret_cast<float4*>(xrows);
+    const int n4 = nr * d / 4;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 8 * blockDim.x) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j * blockDim.x;
+        if (i < n4) v[j] = src[i];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j * blockDim.x;
+        if (i < n4) dst[i] = v[j];
+      }
+    }
+  }
   __syncthreads();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.y * 8 + w;
@@ -851,8 +870,18 @@ __global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (r >= nr) break;
+      // the row's VEC values as float4s (same summation order as scalar reads)
+      float xv[VEC];
 #pragma unroll
-      for (int q = 0; q < VEC; ++q) acc[r] = fmaf(Num<TW>::to_f(wv[q]), xrows[r * d + k0 + q], acc[r]);
+      for (int q4 = 0; q4 < VEC / 4; ++q4) {
+        const float4 x = *reinterpret_cast<const float4*>(xrows + r * d + k0 + 4 * q4);
+        xv[4 * q4] = x.x;
+        xv[4 * q4 + 1] = x.y;
+        xv[4 * q4 + 2] = x.z;
+        xv[4 * q4 + 3] = x.w;
+      }
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) acc[r] = fmaf(Num<TW>::to_f(wv[q]), xv[q], acc[r]);
     }
   }
 #pragma unroll
@@ -951,17 +980,27 @@ __device__ __forceinline__ float entry_gate(float v, int n, int lane) {
 __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, int* __restrict__ topkx,
                             float* __restrict__ gate, int* __restrict__ ecount, int* __restrict__ elist,
                             int* __restrict__ eslot, int B, int E, int k, int ka, int maxB, int select, int prim,
-                            int aux, int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l) {
+                            int aux, int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l, int stage) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kx = aux ? ka - k : 0;  // auxiliary-own experts per token
+  // The router rows of the active flows are read once into shared memory
+  // when they fit (the selection rounds re-read them), else from global.
+  extern __shared__ float rsm[];  // [2B][E] when staged
+  const float* rl = rlog;
+  if (stage) {
+    const int lo = prim ? 0 : B, hi = aux ? 2 * B : B;
+    for (int i = lo * E + (int)threadIdx.x; i < hi * E; i += blockDim.x) rsm[i] = rlog[i];
+    __syncthreads();
+    rl = rsm;
+  }
   // one warp per sequence
   for (int b = w; b < B; b += warps) {
     int sel = 0;  // lane j < k: the j-th replayed expert
     unsigned long long tlo = 0ull, thi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
     if (select) {
-      const float* r = rlog + (size_t)b * E;
+      const float* r = rl + (size_t)b * E;
       for (int j = 0; j < k; ++j) {
         const int bi = warp_pick(r, E, lane, tlo, thi);
         if (lane == 0) topk_l[b * k + j] = bi;
@@ -974,14 +1013,14 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
     }
     // primary gates over the replayed set
     if (prim) {
-      const float* r = rlog + (size_t)b * E;
+      const float* r = rl + (size_t)b * E;
       const float g = entry_gate(lane < k ? r[sel] : -INFINITY, k, lane);
       if (lane < k) gate[(size_t)b * ka + lane] = g;
     }
     // auxiliary: its own experts outside the replayed set, gates over the union
     int own = 0;  // lane k + j: the j-th auxiliary-own expert
     if (aux) {
-      const float* r = rlog + (size_t)(B + b) * E;
+      const float* r = rl + (size_t)(B + b) * E;
       for (int j = 0; j < kx; ++j) {
         const int bi = warp_pick(r, E, lane, tlo, thi);
         if (lane == 0) topkx[b * kx + j] = bi;
@@ -995,7 +1034,7 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
     }
     if (dbg_topk_l && prim && lane < k) dbg_topk_l[b * ka + lane] = sel;
     if (dbg_router_l && prim)
-      for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rlog[(size_t)b * E + e];
+      for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rl[(size_t)b * E + e];
   }
   __syncthreads();
   // entry lists in ascending entry order: warp per expert, 32 entries a round
@@ -1021,10 +1060,12 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
 void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
                       float* dbg_router, cudaStream_t s) {
   int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_route, dim3(1), dim3(1024), 0, s, Bf.rlog, topk_l, Bf.topkx, Bf.gate, Bf.ecount, Bf.elist,
-             Bf.eslot, R.B, D.E, D.k, D.ka, D.maxB, select, R.has_primary(), R.has_aux(),
-             dbg_topk ? dbg_topk + (size_t)layer * R.B * D.ka : nullptr,
-             dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr);
+  const size_t rows_bytes = (size_t)2 * R.B * D.E * sizeof(float);
+  const int stage = rows_bytes <= 40 * 1024 ? 1 : 0;  // within the default dynamic shared memory
+  launch_pdl(k_moe_route, dim3(1), dim3(1024), stage ? rows_bytes : 0, s, (const float*)Bf.rlog, topk_l, Bf.topkx,
+             Bf.gate, Bf.ecount, Bf.elist, Bf.eslot, R.B, D.E, D.k, D.ka, D.maxB, select, R.has_primary(),
+             R.has_aux(), dbg_topk ? dbg_topk + (size_t)layer * R.B * D.ka : nullptr,
+             dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr, stage);
 }
 
 // Expert gate/up + SwiGLU + b coupling (CUDA cores): one warp per expert
