@@ -330,7 +330,7 @@ def kv_spread_bounds(name):
 
 
 def spread_tolerance(name, base):
-    """Full-size tolerance: the benchmark spec bound, or three times the fp64 oracle's
+    """Full-size tolerance: the stated bf16 bound (2e-2), or three times the fp64 oracle's
     own spread under 1e-7 relative perturbations before its bf16 roundings
     (tests/golden/oracle_spread.json), whichever is larger."""
     import json, os

@@ -5,7 +5,7 @@ Tolerance: at these depths and widths the bf16 quantisation points turn
 last-bit differences into rounding flips that cascade through the layers;
 the fp64 oracle itself moves by ~0.04-0.05 in log p when its pre-rounding
 values are perturbed by 1e-7 relative (tests/golden/oracle_spread.json).  The
-log-probability bound is therefore the larger of the benchmark spec bound
+log-probability bound is therefore the larger of the stated bf16 bound
 (2e-2) and three times that measured spread.
 
 The GPU runs the whole batch; the oracle follows sampled sequences (batch
