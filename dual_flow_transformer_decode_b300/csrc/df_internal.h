@@ -91,11 +91,6 @@ struct Buffers {
   int* gen_tok;     // [maxB] generation: the next step's input tokens (written by the draw)
   int* gen_hist;    // [max_len][maxB] generation: the token drawn at each position
   float* rope;      // [max_len][hd/2][2] cos, sin
-  int* tickets;     // split-K tile tickets
-  int* attn_tickets;  // [maxB][Hkv] split-merge tickets of the attention kernel
-  size_t tickets_cap;
-  float* gpart;     // split-K partial tiles
-  size_t gpart_cap; // floats
   void* mk;         // persistent-kernel region (maps, task lists, counters, partials)
   size_t mk_bytes;
   void* bp;         // batched-prefill chunk buffers

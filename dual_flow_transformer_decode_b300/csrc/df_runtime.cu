@@ -260,11 +260,6 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.gen_tok = (int*)take(D.maxB * 4);
   b.gen_hist = (int*)take((size_t)D.max_len * D.maxB * 4);
   b.rope = (float*)take((size_t)(D.max_len + 1) * D.hd * 4);
-  b.tickets_cap = df::tc_tickets_needed(D);
-  b.tickets = (int*)take(b.tickets_cap * 4);
-  b.attn_tickets = (int*)take((size_t)D.maxB * D.Hkv * 4);
-  b.gpart_cap = df::tc_partial_floats(D);
-  b.gpart = (float*)take(b.gpart_cap * 4);
   b.mk_bytes = df::mk_workspace_bytes(D);
   b.mk = b.mk_bytes ? take(b.mk_bytes) : nullptr;
   b.bp_bytes = df::bp_workspace_bytes(D);
