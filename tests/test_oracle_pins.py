@@ -189,3 +189,31 @@ def test_topk_desc_ties_go_to_lower_index():
     for _ in range(50):
         r = np.round(g.standard_normal(64), 1)
         np.testing.assert_array_equal(topk_desc(r, 4), np.argsort(-r, kind="stable")[:4])
+
+
+def test_aux_own_experts_are_the_next_ranks_after_the_replayed_set():
+    """The auxiliary flow's own experts (independent fan-out): with S the
+    primary top-k of the same logits they are ranks k .. k+nx-1 of one stable
+    descending sort; for any other S, brute force over all subsets of the
+    right size that avoid S picks the same set (largest logit sum, then the
+    lexicographically smallest index list).  The reported margin is the gap
+    at the cut."""
+    from itertools import combinations
+    from oracle import Oracle
+    g = np.random.default_rng(12)
+    for _ in range(40):
+        r = np.round(g.standard_normal(12), 1)  # coarse values: many ties
+        order = np.argsort(-r, kind="stable")
+        for k, nx in ((2, 2), (4, 4), (1, 6)):
+            S = topk_desc(r, k)
+            X = Oracle._aux_extra(r, S, nx)
+            np.testing.assert_array_equal(X, order[k:k + nx])
+            assert Oracle._aux_extra_margin(r, S, nx) == r[order[k + nx - 1]] - r[order[k + nx]]
+        S = g.choice(12, size=3, replace=False)
+        rest = [e for e in range(12) if e not in set(S.tolist())]
+        best = min(combinations(rest, 3), key=lambda c: (-sum(r[e] for e in c), sorted(c)))
+        X = Oracle._aux_extra(r, S, 3)
+        assert sorted(X.tolist()) == sorted(best)
+        assert not set(X.tolist()) & set(S.tolist())
+        assert all(r[X[i]] >= r[X[i + 1]] for i in range(len(X) - 1))
+    assert Oracle._aux_extra(r, S, 0).shape == (0,)
