@@ -99,3 +99,30 @@ def test_moe_batched_prefill_workspace(lib):
     small, _ = binding.df_workspace_bytes(binding.make_config(cfg, 5, 40))
     big, _ = binding.df_workspace_bytes(binding.make_config(cfg.with_(expert_hidden=384), 5, 40))
     assert big > small > 0
+
+
+def test_missing_library_fails_loudly():
+    """Without libdf.so every binding call raises instead of computing
+    anything another way (there is no CPU or library fallback; the model
+    wrapper reaches the GPU only through these calls)."""
+    import subprocess
+    import sys
+    code = r'''
+import os
+real = os.path.exists
+os.path.exists = lambda p: False if str(p).endswith("libdf.so") else real(p)
+import dfsynth
+from dual_flow_transformer_decode_b300 import binding
+cfg = dfsynth.get_config("t_fp32")
+for call in (binding.lib,
+             lambda: binding.df_workspace_bytes(binding.make_config(cfg, cfg.batch, cfg.max_len))):
+    try:
+        call()
+    except ImportError as e:
+        assert "libdf.so" in str(e), e
+    else:
+        raise SystemExit("no error without the library")
+print("ok")
+'''
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
