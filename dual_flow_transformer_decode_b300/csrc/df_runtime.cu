@@ -1105,16 +1105,22 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_step_scratch on the current device, looked up once per
-// device.  In host code the symbol is only a host-side stand-in, so the
-// address must come from cudaGetSymbolAddress.
-cudaError_t static_scratch(float** out) {
+// Device address of g_step_scratch on the current device.  In host code the
+// symbol is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress.  It is looked up again on every call made outside
+// stream capture (a device reset in between reloads the module at another
+// address); a call made while `s` is being captured reuses the address
+// found by the last call outside capture on that device.
+cudaError_t static_scratch(cudaStream_t s, float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
     float* p = nullptr;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_step_scratch);
     if (e != cudaSuccess) return e;
@@ -1124,6 +1130,25 @@ cudaError_t static_scratch(float** out) {
   return cudaSuccess;
 }
 
+// Floats of the static array the step will use: the attention partials of
+// the path the step takes.  The TMA attention kernel merges its KV splits
+// in distributed shared memory and needs none; the persistent pass writes
+// segment partials of its own layout; the CUDA-core attention writes one
+// (head_dim + 2)-float partial per (sequence, KV head, split, query row).
+size_t static_scratch_need(df_ctx* X, size_t* parts_out) {
+  const Dims& D = X->D;
+  const size_t parts = (size_t)X->B * D.Hkv * X->splits * 2 * D.G;
+  *parts_out = parts;
+  const int B = X->B;
+  const bool two = X->aux_on && X->ungrouped;
+  const Rows r0 = two ? Rows{B, 0, B} : Rows{B, 0, X->aux_on ? 2 * B : B};
+  const Rows r1 = Rows{B, B, 2 * B};
+  if (!X->force_generic && df::mk_can_run(X->mk, r0) && (!two || df::mk_can_run(X->mk, r1)))
+    return df::mk_attn_partial_floats(D);
+  if (!X->force_generic && df::attn_fast_can_run(X->at, D)) return 0;
+  return parts * (D.hd + 2);
+}
+
 }  // namespace
 
 extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax,
@@ -1131,8 +1156,8 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
   if (!X) return DF_ERR_ARG;
   if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_noalloc: null tokens");
   if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_noalloc before df_prefill");
-  const size_t parts = (size_t)X->B * X->D.Hkv * X->splits * 2 * X->D.G;
-  const size_t need = parts * (X->D.hd + 2);
+  size_t parts = 0;
+  const size_t need = static_scratch_need(X, &parts);
   if (need > kStaticScratchFloats) {
     char buf[160];
     snprintf(buf, sizeof(buf),
@@ -1141,7 +1166,7 @@ extern "C" df_status df_decode_step_noalloc(df_ctx* X, const int32_t* tokens, fl
     return fail(X, DF_ERR_CAPACITY, buf);
   }
   float* scratch = nullptr;
-  cudaError_t e = static_scratch(&scratch);
+  cudaError_t e = static_scratch(X->stream, &scratch);
   if (e != cudaSuccess) return cuda_fail(X, e, "cudaGetSymbolAddress");
   df_status pst = prepare_steps(X, 1, "df_decode_step_noalloc");
   if (pst != DF_OK) return pst;

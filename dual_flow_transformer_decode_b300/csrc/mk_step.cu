@@ -1194,7 +1194,7 @@ Region region_of(const Dims& D) {
   g.cnt = take(g.ncnt * 4, 256);
   g.gregion = (size_t)(MT + S) * kBM * kMaxN;
   g.gpart = take(4 * g.gregion * 4, 256);
-  g.apart = take((size_t)std::min(D.maxB, 16) * D.Hkv * kMaxAttnSeg * kApart * 4, 256);
+  g.apart = take(mk_attn_partial_floats(D) * 4, 256);
   g.total = cur;
   return g;
 }
@@ -1462,6 +1462,10 @@ bool mk_batch(MkPlan& P, const Dims& D, const Buffers& Bf, int B, std::string* e
     rs.built = true;
   }
   return true;
+}
+
+size_t mk_attn_partial_floats(const Dims& D) {
+  return (size_t)std::min(D.maxB, 16) * D.Hkv * kMaxAttnSeg * kApart;
 }
 
 bool mk_can_run(const MkPlan& P, const Rows& R) {

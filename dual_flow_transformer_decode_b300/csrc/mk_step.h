@@ -81,6 +81,9 @@ bool mk_init(MkPlan& P, const Dims& D, const Buffers& Bf, void* region, void* kv
 // Builds the task lists for batch B (synchronous host-to-device copies).
 bool mk_batch(MkPlan& P, const Dims& D, const Buffers& Bf, int B, std::string* err);
 bool mk_can_run(const MkPlan& P, const Rows& R);
+// Floats of attention segment partials a launch may write (the capacity of
+// the plan's region: every row set, every segment count the planner picks).
+size_t mk_attn_partial_floats(const Dims& D);
 // One launch: every layer of a pass over rows R.
 void mk_launch(const MkPlan& P, const Dims& D, const Buffers& Bf, void* kv, const Rows& R, int save, int saved,
                cudaStream_t s);

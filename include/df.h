@@ -209,12 +209,18 @@ df_status df_debug_outputs(df_ctx* ctx, float* logp1, float* logp2, int32_t* top
  * The partials that the split-KV attention kernels exchange are kept in a
  * file-scope device array of 2^20 floats (4 MiB) that every GPU loading the
  * library reserves until the process exits; the workspace given to
- * df_create is still used for everything else.
+ * df_create is still used for everything else.  Which partials the step
+ * writes depends on the attention path it takes: the TMA attention kernel
+ * (bf16, head_dim 128) merges its KV splits in distributed shared memory and
+ * writes none; the CUDA-core attention writes B * n_kv_heads * splits *
+ * 2 * (n_heads/n_kv_heads) rows of head_dim + 2 floats; the persistent pass
+ * (DF_MK=1) writes up to min(max_batch, 16) * n_kv_heads * 16 segments of
+ * 8 * (head_dim + 2) floats.
  *  - Returns DF_ERR_CAPACITY before enqueuing anything when the partials of
- *    the current batch (B * n_kv_heads * splits * 2 * (n_heads/n_kv_heads)
- *    rows of head_dim + 2 floats) exceed the array.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    the path the current batch takes exceed the array.
+ *  - The array's device address is looked up (cudaGetSymbolAddress) on every
+ *    call made outside stream capture, and reused from the last such call
+ *    during capture: make the first call on a device before any capture.
  *  - All calls in the process share the one array and it keeps the last
  *    call's contents (every slot a call reads is written by that call first);
  *    calls that overlap on the GPU, from any context or stream, race. */

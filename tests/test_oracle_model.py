@@ -220,6 +220,114 @@ def test_primary_flow_is_a_standard_transformer(name):
             np.testing.assert_allclose(o.V[l][s][:, :P], Vs[l], rtol=0, atol=1e-12)
 
 
+def _bf16_by_hand(x):
+    """Round fp64 values to the nearest bf16 value, ties to even, in one
+    rounding: frexp gives x = m * 2^e with 0.5 <= |m| < 1, so m * 256 carries
+    exactly bf16's 8 significant bits before the point; torch.round rounds
+    half to even."""
+    m, e = torch.frexp(x)
+    return torch.ldexp(torch.round(m * 256.0) / 256.0, e)
+
+
+def _torch_dualflow_bf16(cfg, w, tok):
+    """Both flows at the last position of tok[n], written out with torch
+    library routines, with every bf16 rounding inserted by hand where the
+    method's bf16 storage puts it: GEMM inputs (normed rows, attention
+    output, MLP hidden), cache stores (K after RoPE, V) and the queries
+    entering attention (after RoPE); residual, norms, couplings, softmax and
+    mixture stay in fp64.  The primary flow runs causally over all n
+    positions; the auxiliary flow runs at the last one only, from E2, with
+    Q2 = Wq u2 + a * q1 (q1 the primary's unrounded pre-RoPE query there),
+    z2 += b * z1 (post-gating, unrounded z1), y2 += c * y1 (before the
+    residual add), attending to the primary's K/V 0..n-1.
+    Returns (log p1, log p2, log p_mix, alpha, K[l], V[l])."""
+    T = lambda k: torch.from_numpy(np.asarray(w[k], dtype=np.float64))  # noqa: E731
+    bf = _bf16_by_hand
+    n = len(tok)
+    hd, Hq, Hkv, d = cfg.head_dim, cfg.n_heads, cfg.n_kv_heads, cfg.d_model
+    x1 = T(("emb1",))[torch.from_numpy(tok.astype(np.int64))]
+    x2 = T(("emb2",))[int(tok[-1])].clone()
+    pos = torch.arange(n, dtype=torch.float64)
+    inv = cfg.rope_theta ** (-torch.arange(hd // 2, dtype=torch.float64) * 2 / hd)
+    rot = torch.polar(torch.ones(n, hd // 2, dtype=torch.float64), pos[:, None] * inv[None])
+
+    def rope_c(v, r):  # v [..][hd] rotated by r [..][hd/2]
+        z = torch.complex(v[..., : hd // 2], v[..., hd // 2:]) * r
+        return torch.cat([z.real, z.imag], -1)
+
+    def norm(x, key):
+        return F.rms_norm(x, (d,), weight=T(key), eps=cfg.norm_eps)
+
+    Ks, Vs = [], []
+    for l in range(cfg.n_layers):
+        u = bf(norm(x1, (l, "attn_norm")))
+        q = u @ T((l, "wq")).T                                            # [n][Hq*hd], pre-RoPE
+        k = (u @ T((l, "wk")).T).view(n, Hkv, hd).transpose(0, 1)
+        v = (u @ T((l, "wv")).T).view(n, Hkv, hd).transpose(0, 1)
+        kr, vr = bf(rope_c(k, rot)), bf(v)
+        Ks.append(kr.numpy())
+        Vs.append(vr.numpy())
+        qr = bf(rope_c(q.view(n, Hq, hd).transpose(0, 1), rot))
+        o1 = F.scaled_dot_product_attention(qr[None], kr[None], vr[None], is_causal=True, enable_gqa=True)[0]
+        u2 = bf(norm(x2, (l, "attn_norm")))
+        Q2 = u2 @ T((l, "wq")).T + T((l, "a")) * q[-1]
+        q2r = bf(rope_c(Q2.view(Hq, 1, hd), rot[-1:]))
+        o2 = F.scaled_dot_product_attention(q2r[None], kr[None], vr[None], enable_gqa=True)[0]
+        x1 = x1 + bf(o1.transpose(0, 1).reshape(n, -1)) @ T((l, "wo")).T
+        x2 = x2 + bf(o2.reshape(-1)) @ T((l, "wo")).T
+        u = bf(norm(x1, (l, "mlp_norm")))
+        z1 = F.silu(u @ T((l, "wg")).T) * (u @ T((l, "wu")).T)
+        y1 = bf(z1) @ T((l, "wd")).T
+        x1 = x1 + y1
+        u2 = bf(norm(x2, (l, "mlp_norm")))
+        z2 = F.silu(u2 @ T((l, "wg")).T) * (u2 @ T((l, "wu")).T) + T((l, "b")) * z1[-1]
+        x2 = x2 + bf(z2) @ T((l, "wd")).T + T((l, "c")) * y1[-1]
+    lp1 = torch.log_softmax(bf(norm(x1[-1], ("final_norm",))) @ T(("lm_head",)).T, -1)
+    lp2 = torch.log_softmax(bf(norm(x2, ("final_norm",))) @ T(("lm_head",)).T, -1)
+    alpha = 0.5 + 0.5 * torch.exp(2 * lp1).sum()
+    lmix = torch.logaddexp(torch.log(alpha) + lp1, torch.log1p(-alpha) + lp2)
+    return lp1.numpy(), lp2.numpy(), lmix.numpy(), float(alpha), Ks, Vs
+
+
+def test_bf16_by_hand_rounds_once_to_nearest_even():
+    # the test's own rounding, against values whose bf16 neighbours are known
+    one = 1.0
+    ulp = 2.0 ** -7                                   # bf16 spacing in [1, 2)
+    x = torch.tensor([one + ulp / 2, one + 1.5 * ulp, one + ulp / 2 + 2.0 ** -40, -(one + ulp / 2),
+                      3.0 * 2.0 ** -130, 0.0], dtype=torch.float64)
+    want = [one, one + 2 * ulp, one + ulp, -one, 3.0 * 2.0 ** -130, 0.0]
+    assert _bf16_by_hand(x).tolist() == want
+    r = torch.randn(10000, dtype=torch.float64) * 7
+    # single rounding agrees with fp32 -> bf16 wherever fp64 -> fp32 is exact
+    r32 = r.float().double()
+    assert torch.equal(_bf16_by_hand(r32), r32.float().to(torch.bfloat16).double())
+
+
+@pytest.mark.parametrize("name", ["t_bf16", "t_bf16_b9"])
+def test_bf16_rounding_points_match_a_hand_written_dual_flow_step(name):
+    """The oracle in bf16 mode against the step written out above with the
+    bf16 roundings placed by hand: a rounding point missing, added or moved
+    (for instance the query rounded before RoPE, or the coupling reading a
+    rounded q1 or z1) changes log p by far more than the tolerance, which
+    only has to absorb fp64 summation order."""
+    cfg = dfsynth.get_config(name)
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    P = cfg.n_prefill + 1
+    o = Oracle(cfg, w, cfg.batch)
+    o.prefill(tok[:, :P - 1])
+    r = o.decode_step(tok[:, P - 1], aux=True)
+    for s in range(cfg.batch):
+        lp1, lp2, lmix, alpha, Ks, Vs = _torch_dualflow_bf16(cfg, w, tok[s, :P])
+        np.testing.assert_allclose(r["logp1"][s], lp1, rtol=0, atol=1e-9)
+        np.testing.assert_allclose(r["logp2"][s], lp2, rtol=0, atol=1e-9)
+        np.testing.assert_allclose(r["logp_mix"][s], lmix, rtol=0, atol=1e-9)
+        assert abs(r["alpha"][s] - alpha) <= 1e-12
+        for l in range(cfg.n_layers):
+            np.testing.assert_array_equal(o.K[l][s][:, :P], Ks[l])
+            np.testing.assert_array_equal(o.V[l][s][:, :P], Vs[l])
+
+
 # ---------------------------------------------------------------- auxiliary fan-out
 
 def _aux_moe_layer0_by_hand(cfg, w, tr_primary, tr_aux, nx_pick):

@@ -2,10 +2,19 @@
 device memory where they step the model (a serving loop held to a fixed
 memory budget after start-up, or code building its own CUDA graph).  Its
 split-attention partials live in a static device array instead of the
-workspace; two steps in a row must give what df_decode_step gives.
+workspace.  The same kernels run on the same inputs, so two steps in a row
+must give exactly what df_decode_step gives, bit for bit.
+
+The cases cover each attention path: the CUDA-core split attention (fp32
+models, and a bf16 model with DF_FORCE_GENERIC=1), whose partials go
+through the static array; the persistent pass (DF_MK=1), whose segment
+partials go there too; and the TMA attention kernel (bf16), which merges
+its splits in distributed shared memory and uses none of it.
 
 Kept in a file of its own, collected last, so a failure here comes after
 every other test has run."""
+
+import os
 
 import numpy as np
 import pytest
@@ -16,24 +25,42 @@ from dfsynth.gen import Weights
 pytestmark = pytest.mark.gpu
 
 
-def _pair(cfg):
+def _pair(cfg, env):
+    """Two contexts over the same weights, created with `env` set (the path
+    switches are read when a context is created), both prefilled."""
     import torch
     from dual_flow_transformer_decode_b300.model import DualFlowModel
     w = Weights(cfg, 0)
     tok = dfsynth.tokens(cfg, 0)
-    ms = [DualFlowModel(cfg, w) for _ in range(2)]
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
+    try:
+        ms = [DualFlowModel(cfg, w) for _ in range(2)]
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
     pre = torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda()
     for m in ms:
         m.prefill(pre)
     return ms, tok
 
 
-@pytest.mark.parametrize("name", ["t_fp32", "t_fp32_gqa", "t_bf16"])
-def test_noalloc_step_matches_decode_step(name, cuda_device):
+@pytest.mark.parametrize("name,env", [
+    ("t_fp32", {}),
+    ("t_fp32_gqa", {}),
+    ("t_bf16", {}),
+    ("t_bf16", {"DF_FORCE_GENERIC": "1"}),
+    ("t_bf16", {"DF_MK": "1"}),
+    ("t_bf16_long", {"DF_FORCE_GENERIC": "1"}),
+], ids=["t_fp32", "t_fp32_gqa", "t_bf16", "t_bf16_generic", "t_bf16_persistent", "t_bf16_long_generic"])
+def test_noalloc_step_matches_decode_step(name, env, cuda_device):
     import torch
     from dual_flow_transformer_decode_b300 import binding as b
     cfg = dfsynth.get_config(name)
-    (ref, st), tok = _pair(cfg)
+    (ref, st), tok = _pair(cfg, env)
     B, V = cfg.batch, cfg.vocab
     outs = []
     for m in (ref, st):
@@ -41,7 +68,6 @@ def test_noalloc_step_matches_decode_step(name, cuda_device):
         am = torch.zeros(B, dtype=torch.int32, device="cuda")
         al = torch.zeros(B, device="cuda")
         outs.append((lp, am, al))
-    tol = 1e-4 if cfg.dtype == "f32" else 2e-2
     for s in range(2):
         t = torch.from_numpy(tok[:, cfg.n_prefill + s].copy()).cuda()
         ref.decode_step(t, *outs[0])
@@ -49,11 +75,12 @@ def test_noalloc_step_matches_decode_step(name, cuda_device):
                                  outs[1][2].data_ptr())
         ref.sync()
         st.sync()
-        d = float((outs[0][0] - outs[1][0]).abs().max())
-        assert d <= tol, (s, d)
-        assert np.array_equal(outs[0][1].cpu().numpy(), outs[1][1].cpu().numpy())
-        assert float((outs[0][2] - outs[1][2]).abs().max()) <= tol
+        for x, y in zip(outs[0], outs[1]):
+            np.testing.assert_array_equal(x.cpu().numpy(), y.cpu().numpy(), err_msg=f"step {s}")
     assert st.length == ref.length == cfg.n_prefill + 2
+    n = cfg.n_prefill + 2
+    np.testing.assert_array_equal(ref.kv_view()[:, :, :B, :, :n].float().cpu().numpy(),
+                                  st.kv_view()[:, :, :B, :, :n].float().cpu().numpy())
     ref.close()
     st.close()
 
