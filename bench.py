@@ -5,8 +5,11 @@
 
 A step is one df_decode_step: both flows of B sequences at one position
 (embedding, every layer, LM head, mixture), teacher-forced from the seed.
-The default workload is the dense ~1B model at batch 16 with the cache
-prefilled to 1023 positions.  With N > 1 (torchrun, one process per GPU)
+The default workload is the largest single-GPU one: the 24-layer dense
+model at batch 128 (256 stacked rows) with the cache prefilled to 4096
+positions, where attention is bound by HBM and the projections by the
+tensor cores.  The same run also times the dense ~1B model at batch 16 and
+context 1023 (key "secondary").  With N > 1 (torchrun, one process per GPU)
 every rank runs an independent replica of the workload: the path shards over
 sequences with no exchange, so the value is the aggregate over ranks and the
 scaling is weak.  Rank 0 prints one JSON line.
@@ -177,6 +180,31 @@ def algorithmic_bytes(cfg, op: str, B: int, t: int, moe_union: float | None = No
     if op == "moe":
         touched = moe_union if moe_union is not None else cfg.n_experts
         return cfg.n_experts * d * esz + touched * 3 * cfg.expert_hidden * d * esz
+    raise KeyError(op)
+
+
+def algorithmic_flops(cfg, op: str, B: int, t: int, moe_union: float | None = None) -> float:
+    """Flops one launch of an operation must do for B sequences at position
+    t: every stacked row (primary and auxiliary) through each projection,
+    except the auxiliary rows' Wk/Wv (the auxiliary flow writes no K/V);
+    shared-KV attention of both flows' query heads over t + 1 positions."""
+    d, qd, kvd, F = cfg.d_model, cfg.q_dim, cfg.kv_dim, cfg.ffn_hidden
+    M = 2 * B
+    if op == "qkv":
+        return 2.0 * (M * qd + B * 2 * kvd) * d
+    if op == "attn":
+        return 8.0 * B * cfg.n_heads * cfg.head_dim * (t + 1)
+    if op == "wo":
+        return 2.0 * M * d * qd
+    if op == "gateup":
+        return 2.0 * M * 2 * F * d
+    if op == "down":
+        return 2.0 * M * d * F
+    if op == "lmhead":
+        return 2.0 * M * cfg.vocab * d
+    if op == "moe":
+        ka = max(cfg.aux_top_k, cfg.top_k)
+        return 2.0 * M * cfg.n_experts * d + 2.0 * B * (cfg.top_k + ka) * 3 * cfg.expert_hidden * d
     raise KeyError(op)
 
 
@@ -416,14 +444,44 @@ def run_ours(args, rank, world, local_rank):
     shares = {o: op_ms[o] * per_step_count[o] for o in ops}
     dom = max(shares, key=shares.get)
     hbm_peak, _, peak_kind = _peaks()
-    bytes_dom = algorithmic_bytes(cfg, dom, B, t_mean + 1, moe_union)
-    achieved = bytes_dom / (op_ms[dom] / 1e3) / 1e9
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": captured_traffic(cfg.name, dom),
-                "peak_source": peak_kind, "ms_per_launch": round(op_ms[dom], 5),
-                "algorithmic_bytes_per_launch": bytes_dom}
+    tc_peak = _bf16_sustained()   # every op is timed inside a seconds-long loop
+    op_roof = {}
+    for o in ops:
+        by = algorithmic_bytes(cfg, o, B, t_mean + 1, moe_union)
+        fl = algorithmic_flops(cfg, o, B, t_mean + 1, moe_union)
+        t_hbm, t_tc = by / (hbm_peak * 1e9), fl / (tc_peak * 1e12)
+        sec = op_ms[o] / 1e3
+        if t_tc > t_hbm:
+            op_roof[o] = {"bound": "tensor", "achieved": round(fl / sec / 1e12, 1), "peak": tc_peak,
+                          "unit": "TFLOP/s", "frac": round(t_tc / sec, 4)}
+        else:
+            op_roof[o] = {"bound": "hbm", "achieved": round(by / sec / 1e9, 1), "peak": hbm_peak,
+                          "unit": "GB/s", "frac": round(t_hbm / sec, 4)}
+        op_roof[o].update({"ms_per_launch": round(op_ms[o], 5), "launches_per_step": per_step_count[o],
+                           "algorithmic_bytes": by, "algorithmic_flops": fl,
+                           "achieved_gbs": round(by / sec / 1e9, 1), "achieved_tflops": round(fl / sec / 1e12, 1)})
+    r = op_roof[dom]
+    roofline = {"kernel": dom, "bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"],
+                "unit": r["unit"], "frac": r["frac"],
+                "traffic": captured_traffic(cfg.name, dom) if r["bound"] == "hbm" else None,
+                "peak_source": peak_kind + (" bf16 sustained" if r["bound"] == "tensor" else " copy"),
+                "ms_per_launch": r["ms_per_launch"], "algorithmic_bytes_per_launch": r["algorithmic_bytes"],
+                "algorithmic_flops_per_launch": r["algorithmic_flops"]}
     sb = step_bytes(cfg, B, t_mean, moe_union)
     step_gbs = sb / (ms_step / 1e3) / 1e9
+    # the step's roofline: its operations run one after another, each bound
+    # by HBM bandwidth or by the tensor pipe, whichever it needs longer
+    bound_ms = sum(per_step_count[o] * max(op_roof[o]["algorithmic_bytes"] / (hbm_peak * 1e9),
+                                           op_roof[o]["algorithmic_flops"] / (tc_peak * 1e12)) for o in ops) * 1e3
+    gemm_ops = [o for o in ops if o not in ("attn", "moe")]
+    g_fl = sum(per_step_count[o] * op_roof[o]["algorithmic_flops"] for o in gemm_ops)
+    g_ms = sum(per_step_count[o] * op_ms[o] for o in gemm_ops)
+    step_roof = {"bound_ms": round(bound_ms, 4), "frac": round(bound_ms / ms_step, 4),
+                 "gemm_phase": {"ops": gemm_ops, "tflop_per_step": round(g_fl / 1e12, 4), "ms_per_step": round(g_ms, 4),
+                                "achieved_tflops": round(g_fl / (g_ms / 1e3) / 1e12, 1), "peak_tflops": tc_peak,
+                                "frac_of_bf16_sustained": round(g_fl / (g_ms / 1e3) / 1e12 / tc_peak, 4)},
+                 "attention_phase": {"ms_per_step": round(per_step_count["attn"] * op_ms["attn"], 4),
+                                     "frac_of_hbm": op_roof["attn"]["frac"]}}
 
     # end to end through the host-buffer entry point (pinned host memory)
     reset()
@@ -458,6 +516,8 @@ def run_ours(args, rank, world, local_rank):
         "step_hbm": {"algorithmic_bytes": sb, "achieved_gbs": round(step_gbs, 1),
                      "frac_of_measured": round(step_gbs / hbm_peak, 4), "frac_of_8tbs": round(step_gbs / 8000, 4)},
         "roofline": roofline,
+        "step_roofline": step_roof,
+        "ops": op_roof,
         "ops_ms_per_launch": {o: round(v, 5) for o, v in op_ms.items()},
         "step_latency": latency,
         "prefill": prefill,
@@ -473,9 +533,55 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, args.seed, budget_s=args.cpu_budget)
     model.close()
+    del model
+    torch.cuda.empty_cache()
+    if world == 1 and args.secondary not in ("none", "", cfg.name):
+        result["secondary"] = run_secondary(args, args.secondary, dev)
     if dist is not None:
         dist.destroy_process_group()
     return result
+
+
+def run_secondary(args, name, dev):
+    """The grouped step of a second workload, timed like the main one (W
+    warm-up steps, K timed steps between synchronised CUDA events, inputs
+    larger than L2) from a cache declared filled to the workload's context;
+    the step's work does not depend on the cache contents."""
+    import torch
+    import dfsynth
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+    cfg = dfsynth.get_config(name)
+    B, P, K, W = cfg.batch, cfg.n_prefill, args.steps, args.warmup
+    model = DualFlowModel(cfg, dfsynth.DeviceWeights(cfg, args.seed, dev), max_batch=B, max_len=P + W + K + 1,
+                          device=dev)
+    model.set_length(B, P)
+    tok = torch.from_numpy(dfsynth.tokens(cfg.with_(n_steps=W + K), args.seed)[:, P:].T.copy()).to(dev)
+    tok_buf = torch.empty(B, dtype=torch.int32, device=dev)
+    lp = torch.empty(B, cfg.vocab, device=dev)
+    am = torch.empty(B, dtype=torch.int32, device=dev)
+    al = torch.empty(B, device=dev)
+    for s in range(W):
+        tok_buf.copy_(tok[s])
+        model.decode_step(tok_buf, lp, am, al)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(model.stream)
+    for s in range(W, W + K):
+        tok_buf.copy_(tok[s])
+        model.decode_step(tok_buf, lp, am, al)
+    e1.record(model.stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / K
+    hbm_peak, _, _ = _peaks()
+    sb = step_bytes(cfg, B, P + W + K // 2, None)
+    out = {"workload": name, "batch": B, "context_at_first_step": P, "ms_per_step": round(ms, 4),
+           "tokens_per_s": round(B / (ms / 1e3), 1), "algorithmic_bytes": sb,
+           "step_hbm_gbs": round(sb / (ms / 1e3) / 1e9, 1), "frac_of_measured": round(sb / (ms / 1e3) / 1e9 / hbm_peak, 4),
+           "kernels_per_step": model.step_kernels, "steps": K, "warmup": W}
+    model.close()
+    del model
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------------- oracle (CPU) arm
@@ -563,7 +669,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=8)
-    ap.add_argument("--config", default="dense1b_ctx1k")
+    ap.add_argument("--config", default="dense24l_b128")
+    ap.add_argument("--secondary", default="dense1b_ctx1k",
+                    help="a second workload timed in the same run (grouped step only); 'none' to skip")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -52,6 +52,10 @@ constexpr int kMaxSplit = 16;           // largest cluster (non-portable size)
 
 struct EpArgs {
   int op;
+  // Failure-detection test hook (0 in normal use): the producer first waits
+  // this many nanoseconds on a barrier nothing arrives on, lets that bounded
+  // wait run out, latches the timeout and issues no copy.
+  unsigned long long stall_ns;
   int lo, hi, B;  // active stacked rows
   int n_out;      // valid output features of the matrix
   // QKV
@@ -299,7 +303,8 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(par + 4 * 64);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* never = done + 1;  // no thread arrives on it (the stall hook's wait)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tslot + 1);  // [0] abort
   float* st = reinterpret_cast<float*>(base);                       // [N][128] partial tile, reuses the ring
 
@@ -320,6 +325,7 @@ __global__ void __launch_bounds__(NT, 1)
       ptx::mbar_init(&empty[s], 1);
     }
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(never, 1);
     flags[0] = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -333,7 +339,13 @@ __global__ void __launch_bounds__(NT, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && ep.stall_ns && !ptx::mbar_wait(never, 0, ep.stall_ns)) {
+    // the test hook's wait ran out before any copy was issued: nothing is in
+    // flight, the MMA issuer sees the flag and stops waiting
+    flags[0] = 1;
+    latch_error(ctrl, kErrTimeout, 103);
+    ptx::grid_dep_wait();
+  } else if (warp == 0 && lane == 0) {
     // TMA producer.  The weights do not depend on the previous kernel, so the
     // first stages' weight tiles are requested before waiting for it.
     const uint64_t pol_w = ptx::policy_evict_first();
@@ -360,9 +372,9 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t idesc = ptx::idesc_bf16_f32(kBM, N);
     for (int i = 0; i < nk; ++i) {
       const int s = i % kStages;
-      if (!ptx::mbar_wait(&full[s], (i / kStages) & 1)) {
+      if (!ptx::mbar_wait_abort(&full[s], (i / kStages) & 1, flags)) {
+        if (!flags[0]) latch_error(ctrl, kErrTimeout, 101);
         flags[0] = 1;
-        latch_error(ctrl, kErrTimeout, 101);
         break;
       }
       ptx::tc_fence_after();
@@ -491,6 +503,8 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   P.enabled = false;
   const char* e = getenv("DF_NO_TC");
   if (e && e[0] == '1') return true;
+  const char* st = getenv("DF_TEST_GEMM_STALL_NS");
+  P.stall_ns = st ? strtoull(st, nullptr, 10) : 0;
   if (!D.bf16) return true;
   if (D.hd != 128) return true;
   if (D.qdim % kBM || D.kvdim % kBM || D.d % kBM || D.d % kBK || D.qdim % kBK) return true;
@@ -589,8 +603,10 @@ EpArgs base_args(const Dims& D, const Buffers& Bf, const Rows& R, TcOp op, int n
   return ep;
 }
 
-void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int K, const EpArgs& ep,
+void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int K, const EpArgs& ep0,
             const Buffers& Bf, cudaStream_t s, int splits) {
+  EpArgs ep = ep0;
+  ep.stall_ns = P.stall_ns;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(tiles_of(n_out) * splits);
   lc.blockDim = dim3(128);

@@ -23,6 +23,9 @@ struct TcPlan {
   std::vector<CUtensorMap> w_qkv, w_o, w_gu, w_d;
   CUtensorMap w_lm;
   CUtensorMap x_u, x_o, x_z;
+  // Failure-detection test hook: DF_TEST_GEMM_STALL_NS at df_create makes
+  // every GEMM launch let one bounded wait run out (see k_tc_gemm).
+  unsigned long long stall_ns = 0;
 };
 
 size_t tc_tickets_needed(const Dims& D);

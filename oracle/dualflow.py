@@ -303,7 +303,7 @@ class Oracle:
         return y, sets, r
 
     # decode ----------------------------------------------------------------------
-    def decode_step(self, tok: np.ndarray, aux: bool = True, trace: bool = False) -> dict:
+    def decode_step(self, tok: np.ndarray, aux: bool = True, trace: bool = False, route=None) -> dict:
         """One decode position t for every sequence.
 
         Primary ("Arquitectura Central", Flujo Primario): a standard causal step
@@ -312,6 +312,16 @@ class Oracle:
         primary through a, b, c, attends to the primary K/V 0..t, writes
         nothing.  Output: the mixture of the two next-token distributions
         ("Mecanismos Clave", Objetivo de Mezcla).
+
+        route: optional comparison hook for MoE models,
+        route(kind, layer, seq, logits, chosen) -> experts to use, called
+        after each routing decision with kind "primary" (the top-k set S) or
+        "aux" (the auxiliary flow's own extra experts).  It lets a comparison
+        follow another implementation through a decision that is a tie at
+        that implementation's precision; the returned set replaces the
+        chosen one in that step's arithmetic, which is otherwise unchanged.
+        The returned indices are recorded in the outputs ("topk",
+        "topk_aux").
         """
         cfg = self.cfg
         tok = np.asarray(tok).reshape(-1)
@@ -351,6 +361,8 @@ class Oracle:
                 sets = []
                 for s in range(self.nb):
                     S = topk_desc(r1[s], cfg.top_k)
+                    if route is not None:
+                        S = np.asarray(route("primary", l, s, r1[s], S), dtype=np.int64)
                     sets.append(S)
                     topk_sets[l, s] = S
                     if cfg.n_experts > cfg.top_k:
@@ -406,6 +418,8 @@ class Oracle:
                     for s in range(self.nb):
                         S = sv["sets"][s]
                         X = self._aux_extra(r2[s], S, nx)
+                        if route is not None and nx > 0:
+                            X = np.asarray(route("aux", l, s, r2[s], X), dtype=np.int64)
                         aux_extra[l, s] = X
                         if nx > 0:
                             aux_margin[l, s] = self._aux_extra_margin(r2[s], S, nx)

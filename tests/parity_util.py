@@ -135,7 +135,7 @@ def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
     tol = TOL[cfg.dtype]
     rep = {"max_dlogp_mix": 0.0, "max_dlogp1": 0.0, "max_dalpha": 0.0, "argmax_mismatch": [],
            "near_ties": [], "invalid_near_ties": [], "topk_mismatch": [], "max_drouter": 0.0,
-           "decisions": 0}
+           "decisions": 0, "argmax_decisions": 0, "argmax_exact": 0}
     for s, (g, o) in enumerate(zip(gpu_steps, ora_steps)):
         nb = o["logp1"].shape[0]
         idx = list(range(nb)) if seq_map is None else seq_map
@@ -148,6 +148,7 @@ def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
             for i, b in enumerate(idx):
                 eps = float(dmix[i].max())
                 rep["decisions"] += 1
+                rep["argmax_decisions"] += 1
                 ga, oa = int(g["argmax"][b]), int(o["argmax"][i])
                 if o["argmax_margin"][i] <= 2 * eps:
                     rep["near_ties"].append(("argmax", s, i, float(o["argmax_margin"][i]), eps))
@@ -155,6 +156,8 @@ def compare_steps(cfg, gpu_steps, ora_steps, seq_map=None):
                         rep["invalid_near_ties"].append(("argmax", s, i, ga, oa))
                 elif ga != oa:
                     rep["argmax_mismatch"].append((s, i, ga, oa, float(o["argmax_margin"][i]), eps))
+                else:
+                    rep["argmax_exact"] += 1
         if cfg.n_experts:
             dr = np.abs(g["router1"][:, idx] - o["router1"])
             rep["max_drouter"] = max(rep["max_drouter"], float(dr.max()))
@@ -320,27 +323,115 @@ def compare_moe_steps(cfg, gpu_steps, ora_steps, seq_map):
     return rep
 
 
-def kv_spread_bounds(name):
-    """Full-size K/V bounds: the small-case bounds, or three times the oracle's
-    own spread on the appended K/V, whichever is larger."""
+class RouteFollower:
+    """Routing hook for Oracle.decode_step that follows the GPU through
+    valid near ties instead of stopping at them.
+
+    At each (layer, token) the oracle's choice is compared with the GPU's:
+    with eps = max |GPU - oracle| over that row's primary router logits, a
+    decision whose oracle margin exceeds 2*eps must match exactly (recorded
+    as a mismatch otherwise, and the oracle keeps its own choice); a
+    decision inside 2*eps is a near tie, where the GPU's choice must be
+    valid (its weakest expert within 2*eps of the oracle's) and is then
+    adopted, so both sides continue on the same computation.  The auxiliary
+    flow's own experts rank its own router logits, which the library does
+    not export; their deviation is bounded by twice the primary row's."""
+
+    def __init__(self, cfg, gpu_steps, seq_map):
+        self.cfg, self.g, self.seq_map = cfg, gpu_steps, seq_map
+        self.step = 0
+        self.rep = {"decisions": 0, "exact": 0, "near_ties": [], "invalid_near_ties": [], "topk_mismatch": [],
+                    "followed": [], "self_inconsistent": [], "max_drouter": 0.0}
+
+    def __call__(self, kind, l, i, r, chosen):
+        g = self.g[self.step]
+        b = self.seq_map[i]
+        k = self.cfg.top_k
+        rg = g["router1"][l, b]
+        if kind == "primary":
+            eps = float(np.abs(rg - r).max())
+            self.rep["max_drouter"] = max(self.rep["max_drouter"], eps)
+            gs = [int(x) for x in g["topk"][l, b]]
+            if gs != topk_of(rg, k):
+                self.rep["self_inconsistent"].append((self.step, l, i))
+            srt = np.sort(r)[::-1]
+            margin = float(srt[k - 1] - srt[k]) if len(r) > k else np.inf
+            ex = [int(x) for x in chosen]
+        else:
+            # eps of the primary row of this token, doubled (see above)
+            eps = 2.0 * float(np.abs(rg - self._r1[(l, i)]).max())
+            gs = [int(x) for x in g["topk_aux"][l, b]]
+            S = set(int(x) for x in g["topk"][l, b])
+            rest = sorted((float(r[e]) for e in range(len(r)) if e not in S), reverse=True)
+            nx = len(chosen)
+            margin = rest[nx - 1] - rest[nx] if len(rest) > nx else np.inf
+            ex = [int(x) for x in chosen]
+        self.rep["decisions"] += 1
+        if margin > 2 * eps:
+            if set(gs) != set(ex):
+                self.rep["topk_mismatch"].append((kind, self.step, l, i, gs, ex, margin, eps))
+            else:
+                self.rep["exact"] += 1
+            out = chosen
+        else:
+            self.rep["near_ties"].append((kind, self.step, l, i, margin, eps))
+            if float(r[ex].min()) - float(r[gs].min()) > 2 * eps:
+                self.rep["invalid_near_ties"].append((kind, self.step, l, i, gs, ex))
+                out = chosen
+            else:
+                if set(gs) != set(ex):
+                    self.rep["followed"].append((kind, self.step, l, i))
+                out = np.array(gs, dtype=np.int64)
+        if kind == "primary":
+            self._r1[(l, i)] = r
+        return out
+
+    def begin_step(self, s):
+        self.step = s
+        self._r1 = {}
+
+
+def oracle_follow_synthetic(cfg, weights, tok, sample, steps, gpu_steps, seed=0):
+    """The MoE oracle on the sampled sequences from the synthetic cache,
+    following the GPU's routing through valid near ties (RouteFollower)."""
+    from dfsynth.gen import synthetic_kv_block
+    o = Oracle(cfg, weights, len(sample), max_len=cfg.max_len)
+    for i, b in enumerate(sample):
+        for l in range(cfg.n_layers):
+            K, V = synthetic_kv_block(cfg, seed, l, b, cfg.n_prefill)
+            o.set_cache(i, l, K, V)
+    o.set_length(cfg.n_prefill)
+    rf = RouteFollower(cfg, gpu_steps, sample)
+    outs = []
+    for s in range(steps):
+        rf.begin_step(s)
+        outs.append(o.decode_step(tok[sample, cfg.n_prefill + s], route=rf))
+    return o, outs, rf.rep
+
+
+SPREAD_FACTOR = 1.5
+
+
+def _spread_record(name):
     import json, os
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_spread.json")
-    rec = json.load(open(path))[name]
-    return max(0.05, 3.0 * rec.get("kv_max", 0.0)), max(2.0 ** -8, 3.0 * rec.get("kv_rel_rms", 0.0))
+    return json.load(open(path))[name]
+
+
+def kv_spread_bounds(name):
+    """Full-size K/V bounds: the small-case bounds, or SPREAD_FACTOR times the
+    largest spread of the appended K/V over the oracle's perturbed runs,
+    whichever is larger."""
+    rec = _spread_record(name)
+    return (max(0.05, SPREAD_FACTOR * rec["kv_max"]), max(2.0 ** -8, SPREAD_FACTOR * rec["kv_rel_rms"]))
 
 
 def spread_tolerance(name, base):
-    """Full-size tolerance: the stated bf16 bound (2e-2), or three times the fp64 oracle's
-    own spread under 1e-7 relative perturbations before its bf16 roundings
-    (tests/golden/oracle_spread.json), whichever is larger."""
-    import json, os
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_spread.json")
-    table = json.load(open(path))
-    rec = table[name]
-    spread = rec["max_dlogp_mix"]
-    if rec.get("pairs_compared", 4) < 4:
-        # MoE: the perturbed oracle itself takes the other branch of most
-        # near-tie routings, leaving too few undiverged pairs to measure a
-        # spread; use the dense model of the same width, depth and attention.
-        spread = max(spread, table["dense1b_ctx1k"]["max_dlogp_mix"])
-    return max(base, 3.0 * spread), spread
+    """Full-size log-probability tolerance: the stated bf16 bound (2e-2), or
+    SPREAD_FACTOR times the largest deviation of the fp64 oracle from itself
+    when every value entering a bf16 rounding is perturbed by up to the
+    GPU's own arithmetic error there (tests/golden/oracle_spread.json),
+    whichever is larger.  Returns (tolerance, spread)."""
+    rec = _spread_record(name)
+    spread = max(rec["max_dlogp_mix"], rec["max_dlogp1"])
+    return max(base, SPREAD_FACTOR * spread), spread

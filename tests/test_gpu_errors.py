@@ -136,3 +136,47 @@ def test_paged_and_generation_argument_errors(cuda_device):
     assert m.seq_lengths()[:2] == [44, -1]
     assert int(out[:, 0].min()) >= 0 and int(out[:, 0].max()) < cfg.vocab
     m.close()
+
+
+def test_bounded_wait_that_runs_out_is_reported(cuda_device):
+    """A bounded device wait that runs out is latched as DF_ERR_TIMEOUT and
+    reported by df_sync, with the CUDA context left usable.  The wait is made
+    to run out on purpose by the GEMM kernel's test hook
+    (DF_TEST_GEMM_STALL_NS, read at df_create): every tensor-core GEMM launch
+    first waits 1 ms on a barrier nothing arrives on, before it issues any
+    copy, then stops; its MMA issuer sees the abort flag and stops waiting
+    too, so no copy or MMA is left in flight.  A fresh context created
+    without the hook then decodes normally and matches the oracle."""
+    import os
+    import torch
+    from dual_flow_transformer_decode_b300 import binding as b
+    from oracle import Oracle
+    cfg = dfsynth.get_config("t_bf16")
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    pre = torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda()
+    x = torch.from_numpy(tok[:, cfg.n_prefill].copy()).cuda()
+    os.environ["DF_TEST_GEMM_STALL_NS"] = "1000000"
+    try:
+        m = _model(cfg)
+    finally:
+        del os.environ["DF_TEST_GEMM_STALL_NS"]
+    m.prefill(pre)          # the batched prefill has its own GEMM kernel: unaffected
+    m.sync()
+    m.decode_step(x)
+    with pytest.raises(b.DFError) as e:
+        m.sync()
+    assert e.value.status == b.DF_ERR_TIMEOUT
+    assert "detail 103" in str(e.value), str(e.value)
+    m.sync()                # reported once: the latch is cleared, the context still answers
+    m.close()
+    m2 = _model(cfg)
+    m2.prefill(pre)
+    lp = torch.zeros(cfg.batch, cfg.vocab, device="cuda")
+    m2.decode_step(x, lp)
+    m2.sync()
+    o = Oracle(cfg, w, cfg.batch)
+    o.prefill(tok[:, :cfg.n_prefill])
+    r = o.decode_step(tok[:, cfg.n_prefill])
+    assert float(np.abs(lp.double().cpu().numpy() - r["logp_mix"]).max()) <= 2e-2
+    m2.close()

@@ -2,11 +2,20 @@
 bench.py times (max_batch = batch, max_len = prefill + decode steps).
 
 Tolerance: at these depths and widths the bf16 quantisation points turn
-last-bit differences into rounding flips that cascade through the layers;
-the fp64 oracle itself moves by ~0.04-0.05 in log p when its pre-rounding
-values are perturbed by 1e-7 relative (tests/golden/oracle_spread.json).  The
+the GPU's fp32-level differences into rounding flips that cascade through
+the layers; the fp64 oracle itself moves by several 1e-2 in log p when its
+pre-rounding values are perturbed by the size of the GPU's own arithmetic
+error there (tests/golden/oracle_spread.json, written by
+tests/golden/make_oracle_spread.py from the oracle alone).  The
 log-probability bound is therefore the larger of the stated bf16 bound
-(2e-2) and three times that measured spread.
+(2e-2) and 1.5 times the largest spread measured that way; the stated 2e-2
+holds on the small parity cases (test_gpu_parity.py).
+
+Integer decisions: every argmax whose oracle margin exceeds twice the
+measured deviation of its row must match exactly, and such exactly-checked
+decisions must make up at least a quarter of all compared ones (so the
+check cannot pass vacuously by calling everything a near tie).  Each test
+prints one PARITY_RECORD line with what it measured.
 
 The GPU runs the whole batch; the oracle follows sampled sequences (batch
 rows are independent: no cross-sequence interaction in dense layers, per-token
@@ -20,8 +29,10 @@ import pytest
 import dfsynth
 from dfsynth.gen import Weights
 
-from parity_util import (GpuRun, oracle_run, oracle_run_synthetic, compare_steps, compare_moe_steps, assert_parity,
-                         kv_compare, assert_kv_close, spread_tolerance, kv_spread_bounds)
+import json
+
+from parity_util import (GpuRun, oracle_run, oracle_run_synthetic, oracle_follow_synthetic, compare_steps,
+                         assert_parity, kv_compare, spread_tolerance, kv_spread_bounds)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -30,6 +41,23 @@ def _weights(cfg):
     w = Weights(cfg, 0)
     w.prefetch()
     return w
+
+
+def _record(name, rep, tol, spread, **extra):
+    """One line with the measured deviations (collected into the design
+    notes) and the decision counts; returns it for assertion messages."""
+    rec = {"workload": name, "max_dlogp_mix": rep["max_dlogp_mix"], "max_dlogp1": rep["max_dlogp1"],
+           "tol": tol, "oracle_spread": spread, "ratio_to_spread": rep["max_dlogp_mix"] / spread if spread else None,
+           "argmax_decisions": rep.get("argmax_decisions"), "argmax_exact": rep.get("argmax_exact"),
+           "near_ties": len(rep["near_ties"]), **extra}
+    line = "PARITY_RECORD " + json.dumps(rec)
+    print(line)
+    return line
+
+
+def _assert_exact_floor(rep, line):
+    n = rep["argmax_decisions"]
+    assert rep["argmax_exact"] >= max(2, n // 4), line
 
 
 def test_full_tiny_fp32(cuda_device):
@@ -48,7 +76,7 @@ def test_full_tiny_fp32(cuda_device):
 
 def test_full_dense1b_ctx1k(cuda_device):
     cfg = dfsynth.get_config("dense1b_ctx1k")
-    steps, sample = 4, [0, 15]
+    steps, sample = 6, [0, 5, 10, 15]
     w = _weights(cfg)
     tok = dfsynth.tokens(cfg, 0)
     g = GpuRun(cfg, w, tok, steps=steps, keep_kv=False, synth_sample=None)
@@ -58,21 +86,21 @@ def test_full_dense1b_ctx1k(cuda_device):
     o, outs = oracle_run(cfg, w, tok[sample], steps=steps)
     rep = compare_steps(cfg, g.steps, outs, seq_map=sample)
     rep["tol"], spread = spread_tolerance(cfg.name, rep["tol"])
-    print({k: v for k, v in rep.items() if not isinstance(v, list)}, "oracle spread", spread)
-    assert_parity(cfg, rep, max_near_tie_frac=None)
     n = cfg.n_prefill + steps
     full = np.zeros((cfg.n_layers, 2, len(sample), cfg.n_kv_heads, n, cfg.head_dim), np.float32)
     for i, b in enumerate(sample):
         full[:, :, i] = gkv[b][:, :, :, :n]
     mx, rel = kv_compare(cfg, full, o, n, list(range(len(sample))))
     kmax, krel = kv_spread_bounds(cfg.name)
-    print("kv", mx, rel, "bounds", kmax, krel)
-    assert mx <= kmax and rel <= krel
+    line = _record(cfg.name, rep, rep["tol"], spread, kv_max=mx, kv_rel_rms=rel, kv_bounds=[kmax, krel])
+    assert_parity(cfg, rep, max_near_tie_frac=None)
+    _assert_exact_floor(rep, line)
+    assert mx <= kmax and rel <= krel, line
 
 
 @pytest.mark.parametrize("name,sample,steps", [
     ("dense1b_ctx32k", [0, 3], 3),
-    ("dense24l_b128", [0, 127], 2),
+    ("dense24l_b128", [0, 42, 85, 127], 3),
 ])
 def test_full_synthetic_context(name, sample, steps, cuda_device):
     cfg = dfsynth.get_config(name)
@@ -83,8 +111,6 @@ def test_full_synthetic_context(name, sample, steps, cuda_device):
     o, outs = oracle_run_synthetic(cfg, w, tok, sample, steps)
     rep = compare_steps(cfg, g.steps, outs, seq_map=sample)
     rep["tol"], spread = spread_tolerance(cfg.name, rep["tol"])
-    print(name, {k: v for k, v in rep.items() if not isinstance(v, list)}, "oracle spread", spread)
-    assert_parity(cfg, rep, max_near_tie_frac=None)
     # the K/V appended by the decode steps
     P = cfg.n_prefill
     mx, ss_d, ss_v = 0.0, 0.0, 0.0
@@ -98,36 +124,45 @@ def test_full_synthetic_context(name, sample, steps, cuda_device):
                 ss_v += float((arr[l][i][:, P:P + steps] ** 2).sum())
     rel = (ss_d / ss_v) ** 0.5
     kmax, krel = kv_spread_bounds(cfg.name)
-    print("kv", mx, rel, "bounds", kmax, krel)
-    assert mx <= kmax and rel <= krel
+    line = _record(cfg.name, rep, rep["tol"], spread, kv_max=mx, kv_rel_rms=rel, kv_bounds=[kmax, krel])
+    assert_parity(cfg, rep, max_near_tie_frac=None)
+    _assert_exact_floor(rep, line)
+    assert mx <= kmax and rel <= krel, line
 
 
-@pytest.mark.parametrize("name", ["moe64e_top4", "moe64e_top4_aux8"])
-def test_full_moe64e_top4(name, cuda_device):
+@pytest.mark.parametrize("name,sample,steps", [
+    ("moe64e_top4", [0, 10, 21, 31], 4),
+    ("moe64e_top4_aux8", [0, 31], 4),
+])
+def test_full_moe64e_top4(name, sample, steps, cuda_device):
     """MoE with router replay at full size, and the variant whose auxiliary
-    flow adds 4 experts of its own (the same model; tolerance from its
-    spread).  Router-logit deviations of the size of the bf16 cascade put
-    some top-k decisions inside the near-tie band; a token whose routing
-    takes the other valid branch follows another computation from there on,
-    so values are compared until then (see parity_util.compare_moe_steps)."""
-    sample, steps = [0, 31], 3
+    flow adds 4 experts of its own (the same model).  Router-logit
+    deviations of the size of the bf16 cascade put some top-k decisions
+    inside twice that deviation; at such a near tie the GPU's choice must be
+    valid, and the oracle then takes the same one (parity_util.RouteFollower)
+    so that every (step, token) pair is compared.  Decisions outside the
+    near-tie band must match exactly."""
     cfg = dfsynth.get_config(name)
     w = Weights(cfg, 0)
     w.prefetch()
     tok = dfsynth.tokens(cfg, 0)
     g = GpuRun(cfg, w, tok, steps=steps, keep_kv=False, synth_sample=sample)
     g.close()
-    o, outs = oracle_run_synthetic(cfg, w, tok, sample, steps)
-    rep = compare_moe_steps(cfg, g.steps, outs, sample)
+    o, outs, route = oracle_follow_synthetic(cfg, w, tok, sample, steps, g.steps)
+    rep = compare_steps(cfg, g.steps, outs, seq_map=sample)
     tol, spread = spread_tolerance("moe64e_top4", 2e-2)
-    print({k: v for k, v in rep.items() if not isinstance(v, list) or k == "diverged_at"}, "tol", tol)
-    assert not rep["self_inconsistent"], rep["self_inconsistent"][:5]
-    assert not rep["topk_mismatch"], rep["topk_mismatch"][:5]
-    assert not rep["invalid_near_ties"], rep["invalid_near_ties"][:5]
+    line = _record(name, rep, tol, spread, routing_decisions=route["decisions"], routing_exact=route["exact"],
+                   routing_near_ties=len(route["near_ties"]), routing_followed=len(route["followed"]),
+                   max_drouter=route["max_drouter"], pairs_compared=len(sample) * steps)
+    assert not route["self_inconsistent"], route["self_inconsistent"][:5]
+    assert not route["topk_mismatch"], route["topk_mismatch"][:5]
+    assert not route["invalid_near_ties"], route["invalid_near_ties"][:5]
     assert not rep["argmax_mismatch"], rep["argmax_mismatch"][:5]
-    assert rep["max_dlogp_mix"] <= tol and rep["max_dlogp1"] <= tol, rep
-    # every token's first layers are compared before any divergence
-    assert rep["decisions"] >= len(sample) * cfg.n_layers // 2
+    assert not rep["invalid_near_ties"], rep["invalid_near_ties"][:5]
+    assert rep["max_dlogp_mix"] <= tol and rep["max_dlogp1"] <= tol, line
+    # most routing decisions lie outside the near-tie band and were checked exactly
+    assert route["exact"] >= route["decisions"] // 2, line
+    _assert_exact_floor(rep, line)
 
 
 def test_full_dense1b_ragged_paged_generation(cuda_device):
