@@ -137,6 +137,15 @@ TEST_CONFIGS = {
     "t_bf16_long": DFConfig("t_bf16_long", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                             head_dim=128, ffn_hidden=512, vocab=600, dtype="bf16",
                             batch=2, n_prefill=1100, n_steps=3, gain_std=0.1),
+    # more than 128 stacked rows: the tensor-core GEMMs take their wide form
+    # (one tile of up to 256 stacked rows per SM); 100 sequences give 200
+    # rows (padded to 208), 128 give exactly 256
+    "t_bf16_b100": DFConfig("t_bf16_b100", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
+                            head_dim=128, ffn_hidden=512, vocab=700, dtype="bf16",
+                            batch=100, n_prefill=20, n_steps=3, gain_std=0.1),
+    "t_bf16_b128": DFConfig("t_bf16_b128", n_layers=2, d_model=384, n_heads=6, n_kv_heads=2,
+                            head_dim=128, ffn_hidden=640, vocab=1000, dtype="bf16",
+                            batch=128, n_prefill=12, n_steps=3, gain_std=0.1),
     "t_moe": DFConfig("t_moe", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                       head_dim=128, ffn_hidden=0, vocab=1000, dtype="bf16",
                       batch=5, n_prefill=33, n_steps=5, n_experts=8, top_k=2,
@@ -158,6 +167,10 @@ VARIANTS = {
     # are uniform in [512, 1535] (mean ~1023, as the headline workload)
     "dense1b_paged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_paged", page_len=64),
     "dense1b_ragged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_ragged", page_len=64, ragged=0.5),
+    # profiling cases: the same models and batches at a short context, so that
+    # a counter capture holds a few GB on the device (weights still exceed L2)
+    "dense24l_b128_ctx256": WORKLOADS["dense24l_b128"].with_(name="dense24l_b128_ctx256", n_prefill=256),
+    "moe64e_top4_ctx256": WORKLOADS["moe64e_top4"].with_(name="moe64e_top4_ctx256", n_prefill=256),
 }
 
 

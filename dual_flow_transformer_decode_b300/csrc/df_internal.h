@@ -67,6 +67,7 @@ struct Buffers {
   float* raw;       // [Mpad][rawN] fp32 GEMM output before the epilogue (CUDA-core path)
   int rawN;
   float* logits;    // [2maxB][V]
+  float* gpart;     // tensor-core GEMM split-K partial tiles reduced through L2 (tc_partial_floats)
   float* part_o;    // attention split partials: [parts][hd]
   float* part_ml;   // [parts][2] (running max, running sum)
   size_t parts_cap; // number of (b, kv head, split, row) partial slots

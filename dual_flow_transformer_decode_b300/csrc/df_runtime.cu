@@ -229,6 +229,7 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.rawN = (int)rawN;
   b.raw = (float*)take(Mpad * rawN * 4);
   b.logits = (float*)take(M2 * D.V * 4);
+  b.gpart = (float*)take(df::tc_partial_floats(D) * 4);
   size_t parts = 0;
   for (int B = 1; B <= D.maxB; ++B) {
     size_t p = (size_t)B * D.Hkv * df::attn_splits(D, B) * 2 * D.G;

@@ -49,6 +49,9 @@ constexpr int kBK = 64;                 // K elements per stage (one 128-byte sw
 constexpr int kBM = 128;                // weight rows per tile (MMA M)
 constexpr int kStageW = kBM * kBK * 2;  // 16 KB
 constexpr int kMaxSplit = 16;           // largest cluster (non-portable size)
+constexpr int kStP = kBM + 4;           // row stride (floats) of the partial tile: rows 4 banks apart
+constexpr int kWideN = 128;             // above this many stacked rows a tile takes a whole SM
+constexpr int kWideKB = 200;            // ring budget of such a tile (the partial tile reuses it)
 
 struct EpArgs {
   int op;
@@ -78,35 +81,88 @@ struct EpArgs {
   int F;
   float* logits;
   int V;
+  // wide tiles with split-K: partial tiles in global memory (L2), one
+  // [N][kStP] tile per (tile, split) of the launch
+  float* gpart;
 };
 
-// Reduced values of one (row, pair) unit: features p and p + 64 of the tile.
-struct Pair {
-  float lo, hi;
+// Reduced values of one (row, quad) unit: features p..p+3 and p+64..p+67 of
+// the tile (p a multiple of 4), i.e. four (p, p + 64) pairs.
+struct Quad {
+  float4 lo, hi;
 };
 
-// Sum of the cluster's partial tiles for row m, features p and p+64, in
-// cluster-rank (K-split) order.  All remote loads are issued before the sum.
-__device__ __forceinline__ Pair reduce_pair(cg::cluster_group& cl, float* st, int S, int m, int p) {
-  if (S == 1) return Pair{st[m * kBM + p], st[m * kBM + p + 64]};
-  float a[kMaxSplit], b[kMaxSplit];
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ float f4get(const float4& v, int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; }
+__device__ __forceinline__ void f4set(float4& v, int k, float x) {
+  if (k == 0) v.x = x;
+  else if (k == 1) v.y = x;
+  else if (k == 2) v.z = x;
+  else v.w = x;
+}
+
+// Sums of the cluster's partial tiles for rows m1 and m2 (each if its flag
+// is set), features p..p+3 and p+64..p+67, in cluster-rank (K-split) order,
+// element by element (the same order for every element as a scalar sum).
+// The partial tiles are the ranks' shared memory (distributed shared
+// memory), or, with gp set, the ranks' tiles in global memory at gp +
+// rank * gstride.  Loads are issued four ranks at a time for both rows
+// before they are added.
+__device__ __forceinline__ void reduce_quads(cg::cluster_group& cl, float* st, int S, int m1, bool has1, int m2,
+                                             bool has2, int p, Quad& q1, Quad& q2, const float* gp, size_t gstride) {
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  q1 = Quad{z, z};
+  q2 = Quad{z, z};
+  if (S == 1) {
+    if (has1)
+      q1 = Quad{*reinterpret_cast<const float4*>(st + m1 * kStP + p),
+                *reinterpret_cast<const float4*>(st + m1 * kStP + p + 64)};
+    if (has2)
+      q2 = Quad{*reinterpret_cast<const float4*>(st + m2 * kStP + p),
+                *reinterpret_cast<const float4*>(st + m2 * kStP + p + 64)};
+    return;
+  }
+  for (int s0 = 0; s0 < S; s0 += 4) {
+    float4 a[4], b[4], c[4], d[4];
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < S) {
-      const float* r = cl.map_shared_rank(st, s);
-      a[s] = r[m * kBM + p];
-      b[s] = r[m * kBM + p + 64];
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < S) {
+        const float* r = gp ? gp + (size_t)(s0 + j) * gstride : cl.map_shared_rank(st, s0 + j);
+        if (has1) {
+          a[j] = *reinterpret_cast<const float4*>(r + m1 * kStP + p);
+          b[j] = *reinterpret_cast<const float4*>(r + m1 * kStP + p + 64);
+        }
+        if (has2) {
+          c[j] = *reinterpret_cast<const float4*>(r + m2 * kStP + p);
+          d[j] = *reinterpret_cast<const float4*>(r + m2 * kStP + p + 64);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (s0 + j < S) {
+        if (has1) {
+          q1.lo = f4add(q1.lo, a[j]);
+          q1.hi = f4add(q1.hi, b[j]);
+        }
+        if (has2) {
+          q2.lo = f4add(q2.lo, c[j]);
+          q2.hi = f4add(q2.hi, d[j]);
+        }
+      }
     }
   }
-  float x = 0.f, y = 0.f;
-#pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    if (s < S) {
-      x += a[s];
-      y += b[s];
-    }
-  }
-  return Pair{x, y};
+}
+
+// SiLU with the fast exponential and division: the product feeds a bf16
+// rounding, far coarser than their few-ulp error.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
 }
 
 // Epilogue parameters of pairs [p0, p1), staged in shared memory:
@@ -144,136 +200,188 @@ __device__ __forceinline__ void stage_params(const EpArgs& ep, float* par, int n
   par[3 * 64 + i] = y;
 }
 
-// Epilogue over the pairs [p0, p1) of a 128-row weight tile starting at
-// output feature n0.  Work unit: (sequence b, pair p); the unit handles the
-// primary row b and the auxiliary row B+b together, so the coupling partner
-// of an auxiliary row is at hand.  Features p and p+64 form a RoPE pair
-// (head_dim 128) or a gate/up pair (SwiGLU tiles interleave 64 gate and 64
-// up rows).
+// Epilogue over the pairs [p0, p1) (multiples of 4) of a 128-row weight tile
+// starting at output feature n0.  Work unit: (sequence b, quad of pairs);
+// the unit handles the primary row b and the auxiliary row B+b together, so
+// the coupling partner of an auxiliary row is at hand.  Features p and p+64
+// form a RoPE pair (head_dim 128) or a gate/up pair (SwiGLU tiles interleave
+// 64 gate and 64 up rows).  Shared, global and cache accesses of a unit are
+// 16-byte (fp32) or 8-byte (bf16) vectors of its four consecutive features.
 __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl, float* st, const float* par,
-                                         int S, int n0, int p0, int p1, int tid, int nthreads) {
-  const int np = p1 - p0;
+                                         int S, int n0, int p0, int p1, int tid, int nthreads, const float* gp,
+                                         size_t gstride) {
+  const int nq = (p1 - p0) >> 2;
   const bool prim = ep.lo < ep.B, aux = ep.hi > ep.B;
   const int B = ep.B;
   // paged mode: every sequence at its own position, so the RoPE angles are
   // read per unit instead of from the staged table
   const bool ragged = ep.km.table != nullptr;
   const int t = ep.op == (int)TcOp::QKV && !ragged ? ep.ctrl->t : 0;
-  for (int u = tid; u < B * np; u += nthreads) {
-    const int b = u / np, pp = u % np, p = p0 + pp;
-    Pair v1{0.f, 0.f}, v2{0.f, 0.f};
-    if (prim) v1 = reduce_pair(cl, st, S, b, p);
-    if (aux) v2 = reduce_pair(cl, st, S, B + b, p);
+  // thread -> unit: consecutive threads take consecutive quads of one row
+  // (contiguous row segments in the partial tiles and in the outputs)
+  for (int u = tid; u < B * nq; u += nthreads) {
+    const int b = u / nq, pp = (u % nq) << 2, p = p0 + pp;
+    Quad v1, v2;
+    reduce_quads(cl, st, S, b, prim, B + b, aux, p, v1, v2, gp, gstride);
     const int g0 = n0 + p, g1 = n0 + p + 64;
-    float c = par[pp], sn = par[64 + pp];
-    const float cx = par[128 + pp], cy = par[192 + pp];
+    float4 c = *reinterpret_cast<const float4*>(par + pp), sn = *reinterpret_cast<const float4*>(par + 64 + pp);
+    const float4 cx = *reinterpret_cast<const float4*>(par + 128 + pp);
+    const float4 cy = *reinterpret_cast<const float4*>(par + 192 + pp);
     switch (ep.op) {
       case (int)TcOp::QKV: {
         int tb = t;
         if (ragged) {
           tb = ep.km.pos[b];
-          const float* cs = ep.rope + (size_t)tb * ep.hd;
-          c = cs[2 * p];
-          sn = cs[2 * p + 1];
+          const float4* cs = reinterpret_cast<const float4*>(ep.rope + (size_t)tb * ep.hd + 2 * p);
+          const float4 c01 = cs[0], c23 = cs[1];  // (cos, sin) of pairs p..p+3
+          c = make_float4(c01.x, c01.z, c23.x, c23.z);
+          sn = make_float4(c01.y, c01.w, c23.y, c23.w);
         }
         if (n0 < ep.qdim) {
           if (prim) {
             if (ep.C.save) {
-              ep.C.q1s[(size_t)b * ep.qdim + g0] = v1.lo;
-              ep.C.q1s[(size_t)b * ep.qdim + g1] = v1.hi;
+              *reinterpret_cast<float4*>(ep.C.q1s + (size_t)b * ep.qdim + g0) = v1.lo;
+              *reinterpret_cast<float4*>(ep.C.q1s + (size_t)b * ep.qdim + g1) = v1.hi;
             }
-            ep.qatt[(size_t)b * ep.qdim + g0] = Num<__nv_bfloat16>::quant(v1.lo * c - v1.hi * sn);
-            ep.qatt[(size_t)b * ep.qdim + g1] = Num<__nv_bfloat16>::quant(v1.hi * c + v1.lo * sn);
+            float4 r0, r1;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float lo = f4get(v1.lo, k), hi = f4get(v1.hi, k), ck = f4get(c, k), sk = f4get(sn, k);
+              f4set(r0, k, Num<__nv_bfloat16>::quant(lo * ck - hi * sk));
+              f4set(r1, k, Num<__nv_bfloat16>::quant(hi * ck + lo * sk));
+            }
+            *reinterpret_cast<float4*>(ep.qatt + (size_t)b * ep.qdim + g0) = r0;
+            *reinterpret_cast<float4*>(ep.qatt + (size_t)b * ep.qdim + g1) = r1;
           }
           if (aux) {
-            float q0, q1;
+            float4 q0 = v1.lo, q1 = v1.hi;
             if (ep.C.saved) {
-              q0 = ep.C.q1s[(size_t)b * ep.qdim + g0];
-              q1 = ep.C.q1s[(size_t)b * ep.qdim + g1];
-            } else {
-              q0 = v1.lo;
-              q1 = v1.hi;
+              q0 = *reinterpret_cast<const float4*>(ep.C.q1s + (size_t)b * ep.qdim + g0);
+              q1 = *reinterpret_cast<const float4*>(ep.C.q1s + (size_t)b * ep.qdim + g1);
             }
-            const float a0 = fmaf(cx, q0, v2.lo), a1 = fmaf(cy, q1, v2.hi);
+            float4 r0, r1;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a0 = fmaf(f4get(cx, k), f4get(q0, k), f4get(v2.lo, k));
+              const float a1 = fmaf(f4get(cy, k), f4get(q1, k), f4get(v2.hi, k));
+              const float ck = f4get(c, k), sk = f4get(sn, k);
+              f4set(r0, k, Num<__nv_bfloat16>::quant(a0 * ck - a1 * sk));
+              f4set(r1, k, Num<__nv_bfloat16>::quant(a1 * ck + a0 * sk));
+            }
             const size_t m = (size_t)(B + b) * ep.qdim;
-            ep.qatt[m + g0] = Num<__nv_bfloat16>::quant(a0 * c - a1 * sn);
-            ep.qatt[m + g1] = Num<__nv_bfloat16>::quant(a1 * c + a0 * sn);
+            *reinterpret_cast<float4*>(ep.qatt + m + g0) = r0;
+            *reinterpret_cast<float4*>(ep.qatt + m + g1) = r1;
           }
         } else if (prim) {
           const bool isk = n0 < ep.qdim + ep.kvdim;
           const int g = (isk ? n0 - ep.qdim : n0 - ep.qdim - ep.kvdim) / ep.hd;
           __nv_bfloat16* P = ep.kv + kv_index(ep.km, ep.Hkv, ep.hd, ep.layer, isk ? 0 : 1, kv_page(ep.km, b, tb), g,
                                               kv_off(ep.km, tb));
+          float4 r0 = v1.lo, r1 = v1.hi;
           if (isk) {
-            P[p] = __float2bfloat16_rn(v1.lo * c - v1.hi * sn);
-            P[p + 64] = __float2bfloat16_rn(v1.hi * c + v1.lo * sn);
-          } else {
-            P[p] = __float2bfloat16_rn(v1.lo);
-            P[p + 64] = __float2bfloat16_rn(v1.hi);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float lo = f4get(v1.lo, k), hi = f4get(v1.hi, k), ck = f4get(c, k), sk = f4get(sn, k);
+              f4set(r0, k, lo * ck - hi * sk);
+              f4set(r1, k, hi * ck + lo * sk);
+            }
           }
+          *reinterpret_cast<uint2*>(P + p) = pack4_bf16(r0.x, r0.y, r0.z, r0.w);
+          *reinterpret_cast<uint2*>(P + p + 64) = pack4_bf16(r1.x, r1.y, r1.z, r1.w);
         }
         break;
       }
       case (int)TcOp::RESID: {
-        // every residual value this unit updates is loaded before any store,
-        // so the loads overlap instead of waiting on each other's stores
-        float* h1 = ep.h + (size_t)b * ep.d;
-        float* h2 = ep.h + (size_t)(B + b) * ep.d;
-        const bool k0 = g0 < ep.n_out, k1 = g1 < ep.n_out;
-        const float a0 = (prim && k0) ? h1[g0] : 0.f, a1 = (prim && k1) ? h1[g1] : 0.f;
-        const float c0 = (aux && k0) ? h2[g0] : 0.f, c1 = (aux && k1) ? h2[g1] : 0.f;
-        if (prim && k0) h1[g0] = a0 + v1.lo;
-        if (prim && k1) h1[g1] = a1 + v1.hi;
-        if (aux && k0) h2[g0] = c0 + v2.lo;
-        if (aux && k1) h2[g1] = c1 + v2.hi;
+        // every residual value this unit updates is loaded before any store
+        // (n_out is a multiple of the tile: all four features are valid)
+        float4* h1 = reinterpret_cast<float4*>(ep.h + (size_t)b * ep.d + g0);
+        float4* h2 = reinterpret_cast<float4*>(ep.h + (size_t)(B + b) * ep.d + g0);
+        const float4 a0 = prim ? h1[0] : float4{}, a1 = prim ? h1[16] : float4{};
+        const float4 c0 = aux ? h2[0] : float4{}, c1 = aux ? h2[16] : float4{};
+        if (prim) {
+          h1[0] = f4add(a0, v1.lo);
+          h1[16] = f4add(a1, v1.hi);
+        }
+        if (aux) {
+          h2[0] = f4add(c0, v2.lo);
+          h2[16] = f4add(c1, v2.hi);
+        }
         break;
       }
       case (int)TcOp::SWIGLU: {
         const int fi = (n0 / kBM) * 64 + p;
-        const float z1 = silu_f(v1.lo) * v1.hi;
+        float4 z1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f4set(z1, k, silu_fast(f4get(v1.lo, k)) * f4get(v1.hi, k));
         if (prim) {
-          if (ep.C.save) ep.C.z1s[(size_t)b * ep.F + fi] = z1;
-          ep.z[(size_t)b * ep.F + fi] = __float2bfloat16_rn(z1);
+          if (ep.C.save) *reinterpret_cast<float4*>(ep.C.z1s + (size_t)b * ep.F + fi) = z1;
+          *reinterpret_cast<uint2*>(ep.z + (size_t)b * ep.F + fi) = pack4_bf16(z1.x, z1.y, z1.z, z1.w);
         }
         if (aux) {
-          const float zp = ep.C.saved ? ep.C.z1s[(size_t)b * ep.F + fi] : z1;
-          const float z2 = fmaf(cx, zp, silu_f(v2.lo) * v2.hi);
-          ep.z[(size_t)(B + b) * ep.F + fi] = __float2bfloat16_rn(z2);
+          const float4 zp = ep.C.saved ? *reinterpret_cast<const float4*>(ep.C.z1s + (size_t)b * ep.F + fi) : z1;
+          float4 z2;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            f4set(z2, k, fmaf(f4get(cx, k), f4get(zp, k), silu_fast(f4get(v2.lo, k)) * f4get(v2.hi, k)));
+          *reinterpret_cast<uint2*>(ep.z + (size_t)(B + b) * ep.F + fi) = pack4_bf16(z2.x, z2.y, z2.z, z2.w);
         }
         break;
       }
       case (int)TcOp::DOWN: {
         // loads first (residual values, saved primary outputs), then stores
-        float* h1 = ep.h + (size_t)b * ep.d;
-        float* h2 = ep.h + (size_t)(B + b) * ep.d;
-        const float* ys = ep.C.y1s + (size_t)b * ep.d;
-        const bool k0 = g0 < ep.n_out, k1 = g1 < ep.n_out;
-        const float a0 = (prim && k0) ? h1[g0] : 0.f, a1 = (prim && k1) ? h1[g1] : 0.f;
-        const float c0 = (aux && k0) ? h2[g0] : 0.f, c1 = (aux && k1) ? h2[g1] : 0.f;
+        float4* h1 = reinterpret_cast<float4*>(ep.h + (size_t)b * ep.d + g0);
+        float4* h2 = reinterpret_cast<float4*>(ep.h + (size_t)(B + b) * ep.d + g0);
+        const float4* ys = reinterpret_cast<const float4*>(ep.C.y1s + (size_t)b * ep.d + g0);
+        const float4 a0 = prim ? h1[0] : float4{}, a1 = prim ? h1[16] : float4{};
+        const float4 c0 = aux ? h2[0] : float4{}, c1 = aux ? h2[16] : float4{};
         const bool sv = aux && ep.C.saved;
-        const float yp0 = (sv && k0) ? ys[g0] : v1.lo, yp1 = (sv && k1) ? ys[g1] : v1.hi;
+        const float4 yp0 = sv ? ys[0] : v1.lo, yp1 = sv ? ys[16] : v1.hi;
         if (prim) {
           if (ep.C.save) {
-            if (k0) ep.C.y1s[(size_t)b * ep.d + g0] = v1.lo;
-            if (k1) ep.C.y1s[(size_t)b * ep.d + g1] = v1.hi;
+            float4* yw = reinterpret_cast<float4*>(ep.C.y1s + (size_t)b * ep.d + g0);
+            yw[0] = v1.lo;
+            yw[16] = v1.hi;
           }
-          if (k0) h1[g0] = a0 + v1.lo;
-          if (k1) h1[g1] = a1 + v1.hi;
+          h1[0] = f4add(a0, v1.lo);
+          h1[16] = f4add(a1, v1.hi);
         }
         if (aux) {
-          if (k0) h2[g0] = c0 + fmaf(cx, yp0, v2.lo);
-          if (k1) h2[g1] = c1 + fmaf(cy, yp1, v2.hi);
+          float4 r0, r1;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            f4set(r0, k, f4get(c0, k) + fmaf(f4get(cx, k), f4get(yp0, k), f4get(v2.lo, k)));
+            f4set(r1, k, f4get(c1, k) + fmaf(f4get(cy, k), f4get(yp1, k), f4get(v2.hi, k)));
+          }
+          h2[0] = r0;
+          h2[16] = r1;
         }
         break;
       }
       case (int)TcOp::LOGITS: {
-        if (g0 < ep.n_out) {
-          if (prim) ep.logits[(size_t)b * ep.V + g0] = v1.lo;
-          if (aux) ep.logits[(size_t)(B + b) * ep.V + g0] = v2.lo;
+        if ((ep.V & 3) == 0 && g1 + 3 < ep.n_out) {
+          // rows 16-byte aligned and all eight features valid
+          if (prim) {
+            *reinterpret_cast<float4*>(ep.logits + (size_t)b * ep.V + g0) = v1.lo;
+            *reinterpret_cast<float4*>(ep.logits + (size_t)b * ep.V + g1) = v1.hi;
+          }
+          if (aux) {
+            *reinterpret_cast<float4*>(ep.logits + (size_t)(B + b) * ep.V + g0) = v2.lo;
+            *reinterpret_cast<float4*>(ep.logits + (size_t)(B + b) * ep.V + g1) = v2.hi;
+          }
+          break;
         }
-        if (g1 < ep.n_out) {
-          if (prim) ep.logits[(size_t)b * ep.V + g1] = v1.hi;
-          if (aux) ep.logits[(size_t)(B + b) * ep.V + g1] = v2.hi;
+        // otherwise (a vocabulary not a multiple of 4, or the last tile)
+        // scalar stores, each checked
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (g0 + k < ep.n_out) {
+            if (prim) ep.logits[(size_t)b * ep.V + g0 + k] = f4get(v1.lo, k);
+            if (aux) ep.logits[(size_t)(B + b) * ep.V + g0 + k] = f4get(v2.lo, k);
+          }
+          if (g1 + k < ep.n_out) {
+            if (prim) ep.logits[(size_t)b * ep.V + g1 + k] = f4get(v1.hi, k);
+            if (aux) ep.logits[(size_t)(B + b) * ep.V + g1 + k] = f4get(v2.hi, k);
+          }
         }
         break;
       }
@@ -298,7 +406,7 @@ __global__ void __launch_bounds__(NT, 1)
   // the epilogue's partial tile [N][128] fp32 reuses the ring; the region is
   // the larger of the two
   size_t region = (size_t)kStages * (kStageW + stage_x);
-  if ((size_t)N * kBM * 4 > region) region = (size_t)N * kBM * 4;
+  if ((size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;
   float* par = reinterpret_cast<float*>(base + region);  // [4][64] epilogue parameters
   uint64_t* full = reinterpret_cast<uint64_t*>(par + 4 * 64);
   uint64_t* empty = full + kMaxStages;
@@ -306,7 +414,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t* never = done + 1;  // no thread arrives on it (the stall hook's wait)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tslot + 1);  // [0] abort
-  float* st = reinterpret_cast<float*>(base);                       // [N][128] partial tile, reuses the ring
+  float* st = reinterpret_cast<float*>(base);                       // [N][kStP] partial tile, reuses the ring
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = (int)cl.num_blocks();
@@ -315,7 +423,15 @@ __global__ void __launch_bounds__(NT, 1)
   const int kb0 = (int)((long long)split * kblocks / S), kb1 = (int)((long long)(split + 1) * kblocks / S);
   const int nk = kb1 - kb0;
   const uint32_t ncols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
-  const int p0 = split * 64 / S, p1 = (split + 1) * 64 / S;
+  // Split tiles reduce through L2 when the tile is wide (more than 128
+  // stacked rows) or has three or more K-splits: pulling the ranks' partial
+  // tiles through distributed shared memory then costs more than writing
+  // each tile to global memory and reading the shares back (measured at 256
+  // rows: epilogue 10 us against 4 us; at 32 rows with 6-8 splits the
+  // launch is 1.1-1.4 us shorter).  Two splits keep the cluster exchange.
+  float* gtile = (S >= 3 || (S > 1 && N > kWideN)) ? ep.gpart + (size_t)tile * S * N * kStP : nullptr;
+  // this rank's share of the tile's 64 (p, p + 64) feature pairs, in quads
+  const int p0 = 4 * (split * 16 / S), p1 = 4 * ((split + 1) * 16 / S);
 
   if (tid == 0) {
     ptx::prefetch_tmap(&tw);
@@ -410,20 +526,35 @@ __global__ void __launch_bounds__(NT, 1)
     // lanes 32 (w % 4) .. +31, warps sharing a lane quarter split the
     // 16-column chunks
     const int quarter = warp & 3, r = quarter * 32 + lane;
-    for (int j0 = (warp >> 2) * 16; j0 < N; j0 += 16 * (NT / 128)) {
-      float v[16];
-      ptx::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + j0, v);
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    // the tile's destination: this CTA's shared memory, or its slot in the
+    // global partials when the split tiles are reduced through L2
+    float* dst = gtile ? gtile + (size_t)split * N * kStP : st;
+    if (N % 32 == 0) {
+      for (int j0 = (warp >> 2) * 32; j0 < N; j0 += 32 * (NT / 128)) {
+        float v[32];
+        ptx::tmem_ld32(trow + j0, v);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) st[(j0 + q) * kBM + r] = v[q];
+        for (int q = 0; q < 32; ++q) dst[(j0 + q) * kStP + r] = v[q];
+      }
+    } else {
+      for (int j0 = (warp >> 2) * 16; j0 < N; j0 += 16 * (NT / 128)) {
+        float v[16];
+        ptx::tmem_ld16(trow + j0, v);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dst[(j0 + q) * kStP + r] = v[q];
+      }
     }
   }
   ptx::tc_fence_before();
-  // Every CTA of the cluster has its partial tile in shared memory after this.
+  // Every CTA of the cluster has its partial tile in shared (or global)
+  // memory after this.
   cl.sync();
   ptx::grid_dep_launch();
-  if (!aborted) epilogue(ep, cl, st, par, S, tile * kBM, p0, p1, tid, NT);
-  // Keep this CTA's shared memory alive until the whole cluster has read it.
-  cl.sync();
+  if (!aborted) epilogue(ep, cl, st, par, S, tile * kBM, p0, p1, tid, NT, gtile, (size_t)N * kStP);
+  // Keep this CTA's shared memory alive until the whole cluster has read it
+  // (partials reduced through L2 leave nothing to wait for).
+  if (!gtile) cl.sync();
   if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
 }
 
@@ -475,6 +606,22 @@ int choose_splits(int n_out, int K, int sms, int per_sm) {
   return s;
 }
 
+// K-splits for a wide tile (more than 128 stacked rows): its footprint
+// allows one CTA per SM, and a cluster must fit in one GPC, so a split count
+// whose clusters the device cannot hold at once (max_clusters[s], measured
+// for this kernel and footprint, less two clusters of headroom for the
+// neighbouring kernels' CTAs that programmatic dependent launch keeps
+// resident) would run in two waves.  The largest split count up to 8 that
+// still gives each split at least two K blocks and fits one wave is taken.
+int choose_splits_wide(int n_out, int K, int sms, const int* max_clusters) {
+  const int tiles = tiles_of(n_out), kb = K / kBK;
+  for (int s = 8; s > 1; --s) {
+    if (kb / s < 2 || tiles * s > sms) continue;
+    if (tiles <= max_clusters[s] - 2) return s;
+  }
+  return 1;
+}
+
 // Ring depth: as many stages as fit in `kb` KB (at least 2).
 int stages_for(int N, int kb = 64) {
   int st = (kb * 1024) / (kStageW + N * kBK * 2);
@@ -485,7 +632,7 @@ int stages_for(int N, int kb = 64) {
 
 size_t smem_bytes(int N, int stages) {
   size_t region = (size_t)stages * (kStageW + N * kBK * 2);
-  if ((size_t)N * kBM * 4 > region) region = (size_t)N * kBM * 4;  // epilogue partial tile
+  if ((size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;  // epilogue partial tile
   return region + 1024 + 4 * 64 * 4 + 256;
 }
 
@@ -495,7 +642,14 @@ int mpad_of(const Dims& D) { return (2 * D.maxB + 15) / 16 * 16; }
 
 size_t tc_tickets_needed(const Dims&) { return 1; }
 
-size_t tc_partial_floats(const Dims&) { return 1; }
+// Global split partials: one [N][kStP] tile per CTA of a split launch, at
+// most two CTAs per SM (one for a wide tile), for every batch up to maxB.
+size_t tc_partial_floats(const Dims& D) {
+  if (!D.bf16 || D.hd != 128) return 0;
+  const size_t mpad = (size_t)mpad_of(D);
+  const size_t narrow = 2 * (mpad < (size_t)kWideN ? mpad : (size_t)kWideN);
+  return (size_t)D.sms * (mpad > narrow ? mpad : narrow) * kStP;
+}
 
 bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector<const void*>& wqkv,
                   const std::vector<const void*>& wo, const std::vector<const void*>& wgu,
@@ -540,6 +694,8 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   cudaFuncSetAttribute(k_tc_gemm<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaFuncSetAttribute(k_tc_gemm<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   cudaFuncSetAttribute(k_tc_gemm<256>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(k_tc_gemm<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaFuncSetAttribute(k_tc_gemm<512>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   P.enabled = true;
   P.dense = !D.E;
   return true;
@@ -552,12 +708,42 @@ bool tc_plan_batch(TcPlan& P, const Dims& D, int B, std::string* err) {
   P.npad = N;
   // the split plan depends on how many CTAs of this N fit on one SM
   P.sms = D.sms;
-  const int per_sm = (int)((227 * 1024) / (smem_bytes(N, stages_for(N)) + 1024));
-  P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms, per_sm);
-  P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms, per_sm);
-  P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms, per_sm);
-  P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits(D.d, D.F, D.sms, per_sm);
-  P.splits[(int)TcOp::LOGITS] = choose_splits(D.V, D.d, D.sms, per_sm);
+  if (N > kWideN) {
+    // clusters of each size the device holds at once at the wide footprint
+    int maxc[9] = {0};
+    const size_t smem = smem_bytes(N, stages_for(N, kWideKB));
+    for (int sz = 1; sz <= 8; ++sz) {
+      cudaLaunchConfig_t lc{};
+      lc.gridDim = dim3(sz);
+      lc.blockDim = dim3(512);
+      lc.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = sz;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      lc.attrs = at;
+      lc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k_tc_gemm<512>, &lc) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      maxc[sz] = n;
+    }
+    P.splits[(int)TcOp::QKV] = choose_splits_wide(D.qkvn, D.d, D.sms, maxc);
+    P.splits[(int)TcOp::RESID] = choose_splits_wide(D.d, D.qdim, D.sms, maxc);
+    P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits_wide(2 * D.F, D.d, D.sms, maxc);
+    P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits_wide(D.d, D.F, D.sms, maxc);
+    P.splits[(int)TcOp::LOGITS] = choose_splits_wide(D.V, D.d, D.sms, maxc);
+  } else {
+    const int per_sm = (int)((227 * 1024) / (smem_bytes(N, stages_for(N)) + 1024));
+    P.splits[(int)TcOp::QKV] = choose_splits(D.qkvn, D.d, D.sms, per_sm);
+    P.splits[(int)TcOp::RESID] = choose_splits(D.d, D.qdim, D.sms, per_sm);
+    P.splits[(int)TcOp::SWIGLU] = D.E ? 1 : choose_splits(2 * D.F, D.d, D.sms, per_sm);
+    P.splits[(int)TcOp::DOWN] = D.E ? 1 : choose_splits(D.d, D.F, D.sms, per_sm);
+    P.splits[(int)TcOp::LOGITS] = choose_splits(D.V, D.d, D.sms, per_sm);
+  }
   bool ok = make_map(&P.x_u, P.u_ptr, D.d, P.mpad, N) && make_map(&P.x_o, P.o_ptr, D.qdim, P.mpad, N);
   if (P.dense) ok = ok && make_map(&P.x_z, P.z_ptr, D.F, P.mpad, N);
   if (!ok && err) *err = "cuTensorMapEncodeTiled failed for an activation buffer";
@@ -600,6 +786,7 @@ EpArgs base_args(const Dims& D, const Buffers& Bf, const Rows& R, TcOp op, int n
   ep.F = D.F;
   ep.logits = Bf.logits;
   ep.V = D.V;
+  ep.gpart = Bf.gpart;
   return ep;
 }
 
@@ -611,9 +798,10 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n
   lc.gridDim = dim3(tiles_of(n_out) * splits);
   lc.blockDim = dim3(128);
   // ~64 KB rings let two GEMM CTAs and a neighbouring kernel's CTA share an
-  // SM; a launch of at most one CTA per SM may use a deeper ring.
+  // SM; a launch of at most one CTA per SM may use a deeper ring, and a wide
+  // tile (its partial tile alone takes half the SM) the deepest.
   const bool one_per_sm = tiles_of(n_out) * splits <= P.sms;
-  const int stages = stages_for(P.npad, one_per_sm ? DF_GEMM_WIDE_KB : 64);
+  const int stages = stages_for(P.npad, P.npad > kWideN ? kWideKB : one_per_sm ? DF_GEMM_WIDE_KB : 64);
   lc.dynamicSmemBytes = smem_bytes(P.npad, stages);
   lc.stream = s;
   cudaLaunchAttribute at[2];
@@ -627,7 +815,11 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n
   lc.numAttrs = 2;
   // a footprint above half the SM already means one CTA per SM: use the
   // wider CTA, whose extra warps share the epilogue
-  if (lc.dynamicSmemBytes > 114 * 1024) {
+  if (P.npad > kWideN) {
+    // 256 stacked rows: 16 warps share the TMEM drain and the epilogue
+    lc.blockDim = dim3(512);
+    cudaLaunchKernelEx(&lc, k_tc_gemm<512>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
+  } else if (lc.dynamicSmemBytes > 114 * 1024) {
     lc.blockDim = dim3(256);
     cudaLaunchKernelEx(&lc, k_tc_gemm<256>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
   } else {
