@@ -32,7 +32,7 @@ from dfsynth.gen import Weights
 import json
 
 from parity_util import (GpuRun, oracle_run, oracle_run_synthetic, oracle_follow_synthetic, compare_steps,
-                         assert_parity, kv_compare, spread_tolerance, kv_spread_bounds)
+                         assert_parity, kv_compare, assert_kv_close, spread_tolerance, kv_spread_bounds)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
