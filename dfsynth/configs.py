@@ -137,6 +137,11 @@ TEST_CONFIGS = {
     "t_bf16_long": DFConfig("t_bf16_long", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                             head_dim=128, ffn_hidden=512, vocab=600, dtype="bf16",
                             batch=2, n_prefill=1100, n_steps=3, gain_std=0.1),
+    # one sequence (2 stacked rows): the small projections run as the
+    # CUDA-core GEMV
+    "t_bf16_b1": DFConfig("t_bf16_b1", n_layers=2, d_model=384, n_heads=6, n_kv_heads=2,
+                          head_dim=128, ffn_hidden=640, vocab=1000, dtype="bf16",
+                          batch=1, n_prefill=70, n_steps=5, gain_std=0.1),
     # more than 128 stacked rows: the tensor-core GEMMs take their wide form
     # (one tile of up to 256 stacked rows per SM); 100 sequences give 200
     # rows (padded to 208), 128 give exactly 256

@@ -18,6 +18,9 @@
 //   O += P · V     P is split into bf16 hi + lo parts and both are applied,
 //                  so P enters with ~16 significant bits (relative error below
 //                  2^-16) — far below the bf16 rounding of o that follows.
+//                  With at most 8 query rows (2G <= 8) the lo parts ride in
+//                  the m16 tile's idle rows 8..15, so one MMA applies both
+//                  parts, and the two halves are added after the last tile.
 // The warps' (m, l, O) are merged in shared memory; the splits are merged
 // through distributed shared memory in split order (rank r merges a slice of
 // the output) and written as bf16 rows of o.  Each query row's result
@@ -49,7 +52,9 @@ constexpr int BOX = TP * 64 * 2;  // one TMA box: 64 positions x 64 dims bf16 = 
 constexpr int STAGE = 4 * BOX;    // K lo, K hi, V lo, V hi = 32 KB
 constexpr int RQ = 16;            // query rows per MMA (m16)
 constexpr int kMaxSplits = 16;    // cluster size limit
-constexpr int kLaunchStages = 2;  // ring stages of a launch
+constexpr int kShortStages = 2;   // ring stages when a split has few tiles
+constexpr int kLongStages = 3;    // ... and when it has at least kLongTiles
+constexpr int kLongTiles = 8;
 constexpr float kScale = 0.08838834764831845f;  // 1/sqrt(128)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -96,7 +101,7 @@ __device__ __forceinline__ uint32_t sw_off(int pos, int dim) {
 __global__ void __launch_bounds__(160, 2)
     k_attn_tma(const __grid_constant__ CUtensorMap tkv, const float* __restrict__ qatt, Ctrl* __restrict__ ctrl,
                __nv_bfloat16* __restrict__ out, int B, int Hkv, int G, KvMap km, int layer, int flo, int fhi,
-               int NS, int l2pf) {
+               int NS, int l2pf, int fold) {
   extern __shared__ uint8_t smem_raw[];
   cg::cluster_group cl = cg::this_cluster();
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,11 +270,13 @@ __global__ void __launch_bounds__(160, 2)
         mma_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b00, b01);
         mma_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b10, b11);
       }
-      // ---- online softmax for rows gq (c0, c1) and gq+8 (c2, c3)
+      // ---- online softmax for rows gq (c0, c1) and gq+8 (c2, c3); with
+      // fold, rows gq + 8 hold no query and are skipped
       const int pbase = s0 + it * TP + warp * 16 + 2 * tq;
-      float corr[2];
+      float corr[2] = {1.f, 1.f};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
+        if (fold && h == 1) break;
         float v[4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -303,26 +310,54 @@ __global__ void __launch_bounds__(160, 2)
       split_pair(sc[0][2], sc[0][3], ph[1], pl[1]);  // row gq+8
       split_pair(sc[1][0], sc[1][1], ph[2], pl[2]);  // row gq,   positions 8+2tq..
       split_pair(sc[1][2], sc[1][3], ph[3], pl[3]);  // row gq+8
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        o[j][0] *= corr[0];
-        o[j][1] *= corr[0];
-        o[j][2] *= corr[1];
-        o[j][3] *= corr[1];
-      }
-      // ---- O += P V: V^T fragments by ldmatrix.trans, two 8-dim n-tiles per load
       const int vpos = warp * 16 + (mq & 1) * 8 + r8;
+      if (fold) {
+        // At most 8 query rows: the lo part of row gq takes the MMA's
+        // otherwise idle row gq + 8, so one MMA applies both parts (rows
+        // gq + 8 accumulate lo * V; they are added to rows gq at the end).
 #pragma unroll
-      for (int j2 = 0; j2 < 8; ++j2) {
-        uint32_t v00, v01, v10, v11;
-        ldsm_x4_t(vbase + sw_off(vpos, j2 * 16 + (mq >> 1) * 8), v00, v01, v10, v11);
-        mma_16816(o[2 * j2], ph[0], ph[1], ph[2], ph[3], v00, v01);
-        mma_16816(o[2 * j2], pl[0], pl[1], pl[2], pl[3], v00, v01);
-        mma_16816(o[2 * j2 + 1], ph[0], ph[1], ph[2], ph[3], v10, v11);
-        mma_16816(o[2 * j2 + 1], pl[0], pl[1], pl[2], pl[3], v10, v11);
+        for (int j = 0; j < 16; ++j) {
+          o[j][0] *= corr[0];
+          o[j][1] *= corr[0];
+          o[j][2] *= corr[0];
+          o[j][3] *= corr[0];
+        }
+        // ---- O += P V: V^T fragments by ldmatrix.trans, two 8-dim n-tiles per load
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) {
+          uint32_t v00, v01, v10, v11;
+          ldsm_x4_t(vbase + sw_off(vpos, j2 * 16 + (mq >> 1) * 8), v00, v01, v10, v11);
+          mma_16816(o[2 * j2], ph[0], pl[0], ph[2], pl[2], v00, v01);
+          mma_16816(o[2 * j2 + 1], ph[0], pl[0], ph[2], pl[2], v10, v11);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          o[j][0] *= corr[0];
+          o[j][1] *= corr[0];
+          o[j][2] *= corr[1];
+          o[j][3] *= corr[1];
+        }
+#pragma unroll
+        for (int j2 = 0; j2 < 8; ++j2) {
+          uint32_t v00, v01, v10, v11;
+          ldsm_x4_t(vbase + sw_off(vpos, j2 * 16 + (mq >> 1) * 8), v00, v01, v10, v11);
+          mma_16816(o[2 * j2], ph[0], ph[1], ph[2], ph[3], v00, v01);
+          mma_16816(o[2 * j2], pl[0], pl[1], pl[2], pl[3], v00, v01);
+          mma_16816(o[2 * j2 + 1], ph[0], ph[1], ph[2], ph[3], v10, v11);
+          mma_16816(o[2 * j2 + 1], pl[0], pl[1], pl[2], pl[3], v10, v11);
+        }
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);
+    }
+    if (fold) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] += o[j][2];
+        o[j][1] += o[j][3];
+        o[j][2] = o[j][3] = 0.f;
+      }
     }
     // row sums over the four lanes of a row
 #pragma unroll
@@ -479,7 +514,7 @@ bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err) {
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(sp, 1, 1);
     lc.blockDim = dim3(160);
-    lc.dynamicSmemBytes = smem_bytes(kLaunchStages);
+    lc.dynamicSmemBytes = smem_bytes(kLongStages);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = sp;
@@ -534,10 +569,15 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(splits, D.Hkv, R.B);
   lc.blockDim = dim3(160);
-  // Two ring stages: deeper rings or L2 prefetch of the split measured no
-  // faster, and two stages let two attention CTAs share an SM with a CTA of
-  // the next GEMM.
-  const int ns = kLaunchStages, l2pf = 0;
+  // Ring depth from the tiles a split streams (over the context capacity,
+  // so one captured launch serves every position): three 32 KB stages when
+  // a split has at least kLongTiles tiles (measured, 4096 positions at
+  // batch 128: 173.6 -> 166.5 us; 32768 positions: 52.9 -> 48.1 us), two
+  // for short splits (1023 positions in 4 splits: 13.0 against 13.2 us);
+  // both let two attention CTAs share an SM.  L2 prefetch of the split
+  // measured no faster.
+  const int tiles_per_split = ((D.max_len + TP - 1) / TP + splits - 1) / splits;
+  const int ns = tiles_per_split >= kLongTiles ? kLongStages : kShortStages, l2pf = 0;
   lc.dynamicSmemBytes = smem_bytes(ns);
   lc.stream = s;
   cudaLaunchAttribute at[2];
@@ -549,8 +589,11 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   lc.attrs = at;
   lc.numAttrs = 2;
+  // fold depends on the model only (2G query rows with both flows), never
+  // on which flows are active, so a row's arithmetic is the same either way
+  const int fold = 2 * D.G <= 8 ? 1 : 0;
   cudaLaunchKernelEx(&lc, k_attn_tma, P.kv, (const float*)Bf.qatt, Bf.ctrl, (__nv_bfloat16*)Bf.o, R.B, D.Hkv, D.G,
-                     Bf.kvm, layer, flo, fhi, ns, l2pf);
+                     Bf.kvm, layer, flo, fhi, ns, l2pf, fold);
 }
 
 }  // namespace df

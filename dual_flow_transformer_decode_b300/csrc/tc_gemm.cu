@@ -558,6 +558,153 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
 }
 
+// CUDA-core GEMV for a few stacked rows (2B <= kGemvRows), with the same
+// fused epilogues.  At so few rows a projection is a weight stream with a
+// handful of multiply-adds per weight, so instead of K-splits (and their
+// reduction) the weight matrix is divided finer along its output features:
+// one CTA takes 8 feature pairs (p, p + 64) of a 128-row tile over the whole
+// K range, i.e. 16 weight rows.  Its 256 threads form 4 row groups (4 weight
+// rows each) x 64 K lanes; a K lane streams 16-byte chunks (8 bf16) k = 8c
+// for c = lane, lane + 64, ... of its 4 rows, two chunks in flight, and
+// multiplies each with the same chunk of every stacked row, so a weight is
+// read from HBM once and the activations (a few KB, L1/L2-resident) four
+// times per chunk.  Sums: per lane in k order, then a butterfly over the 32
+// lanes of a warp, then the two warps of a row group in order -- the same
+// order for every output, whatever rows are active.  The first chunks'
+// weights are loaded before griddepcontrol.wait.
+constexpr int kGemvRows = 8;     // most stacked rows the kernel takes
+// Crossover against the tensor-core tile, measured on one B300 (dense ~1B
+// model, microseconds per launch, tensor-core / GEMV): 2 stacked rows QKV
+// 7.3 / 5.5, Wo 6.5 / 5.0, gate/up 15.4 / 20.0, down 11.5 / 13.9, LM head
+// 24.7 / 33.2; 4 rows QKV 7.4 / 7.4, Wo 6.5 / 6.7 and every larger matrix
+// slower; 8 rows slower everywhere.  The GEMV therefore takes 2 stacked rows
+// (one sequence) and matrices of at most kGemvMaxElems weights, where its
+// CTAs stream their 16 rows in one wave; above that the per-CTA fixed cost
+// of several waves outweighs the split-K reduction it avoids.
+constexpr long long kGemvMaxElems = 8ll << 20;
+constexpr int kGemvThreads = 256;
+
+__device__ __forceinline__ void fma8(float& acc, const uint4& w, const uint4& x) {
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&w);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(a[i]), fb = __bfloat1622float2(b[i]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+}
+
+__global__ void __launch_bounds__(kGemvThreads, 2)
+    k_gemv(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ X, int K, int nr, EpArgs ep,
+           Ctrl* ctrl) {
+  __shared__ __align__(16) float st[kGemvRows * kStP];   // [row][kStP] like the tensor-core partial tile
+  __shared__ __align__(16) float par[4 * 64];
+  __shared__ float red[4][2][32];
+  cg::cluster_group cl = cg::this_cluster();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (ep.stall_ns) {
+    // failure-detection test hook (see EpArgs::stall_ns): a bounded wait on a
+    // barrier nothing arrives on runs out; nothing is in flight
+    __shared__ uint64_t never;
+    if (tid == 0) {
+      ptx::mbar_init(&never, 1);
+      ptx::fence_barrier_init();
+      if (!ptx::mbar_wait(&never, 0, ep.stall_ns)) latch_error(ctrl, kErrTimeout, 104);
+    }
+    __syncthreads();
+    ptx::grid_dep_wait();
+    return;
+  }
+  const int tile = blockIdx.x >> 3, q = blockIdx.x & 7;
+  const int n0 = tile * kBM, p0 = 8 * q;
+  const int g = warp >> 1, kl = (warp & 1) * 32 + lane;  // row group, K lane
+  // the group's 4 weight rows: features p0 + 4g' + i of the tile, where the
+  // first two groups take features p0..p0+7 and the last two p0+64..p0+71
+  const int fbase = (g < 2 ? p0 + 4 * g : 64 + p0 + 4 * (g - 2));
+  const __nv_bfloat16* wr[4];
+  bool wv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    wv[i] = n0 + fbase + i < ep.n_out;
+    wr[i] = W + (size_t)(wv[i] ? n0 + fbase + i : 0) * K;
+  }
+  const int nk8 = K >> 3;
+  float acc[4][kGemvRows];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int m = 0; m < kGemvRows; ++m) acc[i][m] = 0.f;
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  // weights of the first two chunks do not depend on the previous kernel
+  uint4 w0[4], w1[4];
+  int c = kl;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w0[i] = (c < nk8 && wv[i]) ? __ldg(reinterpret_cast<const uint4*>(wr[i]) + c) : z4;
+    w1[i] = (c + 64 < nk8 && wv[i]) ? __ldg(reinterpret_cast<const uint4*>(wr[i]) + c + 64) : z4;
+  }
+  if (tid < 64) stage_params(ep, par, n0, p0, 8, tid);
+  ptx::grid_dep_wait();
+  for (; c < nk8; c += 128) {
+    // the next two chunks' weights are requested before this pair is used
+    uint4 n0w[4], n1w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      n0w[i] = (c + 128 < nk8 && wv[i]) ? __ldg(reinterpret_cast<const uint4*>(wr[i]) + c + 128) : z4;
+      n1w[i] = (c + 192 < nk8 && wv[i]) ? __ldg(reinterpret_cast<const uint4*>(wr[i]) + c + 192) : z4;
+    }
+    const bool c1 = c + 64 < nk8;
+#pragma unroll
+    for (int m = 0; m < kGemvRows; ++m) {
+      if (m < nr) {
+        const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)m * K);
+        const uint4 x0 = xr[c], x1 = c1 ? xr[c + 64] : z4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          fma8(acc[i][m], w0[i], x0);
+          fma8(acc[i][m], w1[i], x1);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w0[i] = n0w[i];
+      w1[i] = n1w[i];
+    }
+  }
+  ptx::grid_dep_launch();
+  // butterfly reduce-scatter over the warp: 32 values (4 rows x 8 stacked
+  // rows, v = 8 i + m) leave lane l holding the warp's sum of value l
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int m = 0; m < kGemvRows; ++m) v[8 * i + m] = acc[i][m];
+#pragma unroll
+  for (int o = 16, len = 32; o >= 1; o >>= 1, len >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < len / 2) {
+        const float send = upper ? v[j] : v[j + len / 2];
+        const float keep = upper ? v[j + len / 2] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+  }
+  red[g][warp & 1][lane] = v[0];
+  __syncthreads();
+  if (tid < 128) {
+    const int gg = tid >> 5, vv = tid & 31, i = vv >> 3, m = vv & 7;
+    const float sum = red[gg][0][vv] + red[gg][1][vv];
+    const int f = (gg < 2 ? p0 + 4 * gg : 64 + p0 + 4 * (gg - 2)) + i;
+    st[m * kStP + f] = sum;
+  }
+  __syncthreads();
+  epilogue(ep, cl, st, par, 1, n0, p0, p0 + 8, tid, kGemvThreads, nullptr, 0);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -659,6 +806,8 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   if (e && e[0] == '1') return true;
   const char* st = getenv("DF_TEST_GEMM_STALL_NS");
   P.stall_ns = st ? strtoull(st, nullptr, 10) : 0;
+  const char* gr = getenv("DF_GEMV_ROWS");
+  P.gemv_max_rows = gr ? atoi(gr) : 2;
   if (!D.bf16) return true;
   if (D.hd != 128) return true;
   if (D.qdim % kBM || D.kvdim % kBM || D.d % kBM || D.d % kBK || D.qdim % kBK) return true;
@@ -704,6 +853,15 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
 bool tc_plan_batch(TcPlan& P, const Dims& D, int B, std::string* err) {
   P.B = B;
   if (!P.enabled) return true;
+  // Few stacked rows: the CUDA-core GEMV for the matrices where it measured
+  // faster than the tensor-core tile (see gemv_max_rows)
+  const bool few = 2 * B <= P.gemv_max_rows && 2 * B <= kGemvRows;
+  auto small = [&](long long n_out, long long K) { return n_out * K <= kGemvMaxElems; };
+  P.gemv[(int)TcOp::QKV] = few && small(D.qkvn, D.d);
+  P.gemv[(int)TcOp::RESID] = few && small(D.d, D.qdim);
+  P.gemv[(int)TcOp::SWIGLU] = few && !D.E && small(2LL * D.F, D.d);
+  P.gemv[(int)TcOp::DOWN] = few && !D.E && small(D.d, D.F);
+  P.gemv[(int)TcOp::LOGITS] = few && small(D.V, D.d);
   int N = (2 * B + 15) / 16 * 16;
   P.npad = N;
   // the split plan depends on how many CTAs of this N fit on one SM
@@ -790,10 +948,16 @@ EpArgs base_args(const Dims& D, const Buffers& Bf, const Rows& R, TcOp op, int n
   return ep;
 }
 
-void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, int n_out, int K, const EpArgs& ep0,
-            const Buffers& Bf, cudaStream_t s, int splits) {
+void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, const void* w, const void* x, int n_out,
+            int K, const EpArgs& ep0, const Buffers& Bf, cudaStream_t s, int splits) {
   EpArgs ep = ep0;
   ep.stall_ns = P.stall_ns;
+  if (P.gemv[ep.op]) {
+    // a few stacked rows: CUDA-core GEMV, 8 feature pairs per CTA, no split
+    launch_pdl(k_gemv, dim3(tiles_of(n_out) * 8), dim3(kGemvThreads), 0, s,
+               static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(x), K, 2 * P.B, ep, Bf.ctrl);
+    return;
+  }
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(tiles_of(n_out) * splits);
   lc.blockDim = dim3(128);
@@ -837,14 +1001,14 @@ void tc_qkv(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, co
   ep.C = C;
   ep.kv = (__nv_bfloat16*)kv;
   ep.layer = layer;
-  launch(P, P.w_qkv[layer], P.x_u, D.qkvn, D.d, ep, Bf, s, P.splits[(int)TcOp::QKV]);
+  launch(P, P.w_qkv[layer], P.x_u, w, P.u_ptr, D.qkvn, D.d, ep, Bf, s, P.splits[(int)TcOp::QKV]);
 }
 
 void tc_resid(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const Rows& R,
               cudaStream_t s) {
   (void)w;
   EpArgs ep = base_args(D, Bf, R, TcOp::RESID, D.d);
-  launch(P, P.w_o[layer], P.x_o, D.d, D.qdim, ep, Bf, s, P.splits[(int)TcOp::RESID]);
+  launch(P, P.w_o[layer], P.x_o, w, P.o_ptr, D.d, D.qdim, ep, Bf, s, P.splits[(int)TcOp::RESID]);
 }
 
 void tc_swiglu(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* bvec,
@@ -853,7 +1017,7 @@ void tc_swiglu(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w,
   EpArgs ep = base_args(D, Bf, R, TcOp::SWIGLU, 2 * D.F);
   ep.bvec = bvec;
   ep.C = C;
-  launch(P, P.w_gu[layer], P.x_u, 2 * D.F, D.d, ep, Bf, s, P.splits[(int)TcOp::SWIGLU]);
+  launch(P, P.w_gu[layer], P.x_u, w, P.u_ptr, 2 * D.F, D.d, ep, Bf, s, P.splits[(int)TcOp::SWIGLU]);
 }
 
 void tc_down(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, int layer, const float* cvec,
@@ -862,13 +1026,13 @@ void tc_down(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, i
   EpArgs ep = base_args(D, Bf, R, TcOp::DOWN, D.d);
   ep.cvec = cvec;
   ep.C = C;
-  launch(P, P.w_d[layer], P.x_z, D.d, D.F, ep, Bf, s, P.splits[(int)TcOp::DOWN]);
+  launch(P, P.w_d[layer], P.x_z, w, P.z_ptr, D.d, D.F, ep, Bf, s, P.splits[(int)TcOp::DOWN]);
 }
 
 void tc_logits(const TcPlan& P, const Dims& D, const Buffers& Bf, const void* w, const Rows& R, cudaStream_t s) {
   (void)w;
   EpArgs ep = base_args(D, Bf, R, TcOp::LOGITS, D.V);
-  launch(P, P.w_lm, P.x_u, D.V, D.d, ep, Bf, s, P.splits[(int)TcOp::LOGITS]);
+  launch(P, P.w_lm, P.x_u, w, P.u_ptr, D.V, D.d, ep, Bf, s, P.splits[(int)TcOp::LOGITS]);
 }
 
 }  // namespace df

@@ -26,6 +26,11 @@ struct TcPlan {
   // Failure-detection test hook: DF_TEST_GEMM_STALL_NS at df_create makes
   // every GEMM launch let one bounded wait run out (see k_tc_gemm).
   unsigned long long stall_ns = 0;
+  // Stacked rows up to which the small projections run as a CUDA-core GEMV
+  // instead of tensor-core tiles (measured crossover: 2; DF_GEMV_ROWS
+  // overrides, at most 8), and which ops of this batch take it.
+  int gemv_max_rows = 2;
+  bool gemv[5] = {false, false, false, false, false};
 };
 
 size_t tc_tickets_needed(const Dims& D);

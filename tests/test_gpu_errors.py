@@ -138,20 +138,22 @@ def test_paged_and_generation_argument_errors(cuda_device):
     m.close()
 
 
-def test_bounded_wait_that_runs_out_is_reported(cuda_device):
+@pytest.mark.parametrize("name", ["t_bf16_b1", "t_bf16_b9"])
+def test_bounded_wait_that_runs_out_is_reported(name, cuda_device):
     """A bounded device wait that runs out is latched as DF_ERR_TIMEOUT and
     reported by df_sync, with the CUDA context left usable.  The wait is made
-    to run out on purpose by the GEMM kernel's test hook
-    (DF_TEST_GEMM_STALL_NS, read at df_create): every tensor-core GEMM launch
-    first waits 1 ms on a barrier nothing arrives on, before it issues any
-    copy, then stops; its MMA issuer sees the abort flag and stops waiting
-    too, so no copy or MMA is left in flight.  A fresh context created
+    to run out on purpose by the GEMM kernels' test hook
+    (DF_TEST_GEMM_STALL_NS, read at df_create): every projection launch (the
+    tensor-core GEMM, or the few-row GEMV at one sequence) first waits 1 ms on
+    a barrier nothing arrives on, before it issues any copy, then stops; the
+    tensor-core MMA issuer sees the abort flag and stops waiting too, so no
+    copy or MMA is left in flight.  A fresh context created
     without the hook then decodes normally and matches the oracle."""
     import os
     import torch
     from dual_flow_transformer_decode_b300 import binding as b
     from oracle import Oracle
-    cfg = dfsynth.get_config("t_bf16")
+    cfg = dfsynth.get_config(name)
     w = Weights(cfg, 0)
     tok = dfsynth.tokens(cfg, 0)
     pre = torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda()
@@ -167,7 +169,9 @@ def test_bounded_wait_that_runs_out_is_reported(cuda_device):
     with pytest.raises(b.DFError) as e:
         m.sync()
     assert e.value.status == b.DF_ERR_TIMEOUT
-    assert "detail 103" in str(e.value), str(e.value)
+    # 104: the few-row GEMV (one sequence); 103: the tensor-core GEMM's
+    # producer (9 sequences)
+    assert f"detail {104 if cfg.batch == 1 else 103}" in str(e.value), str(e.value)
     m.sync()                # reported once: the latch is cleared, the context still answers
     m.close()
     m2 = _model(cfg)
