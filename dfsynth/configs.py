@@ -172,10 +172,12 @@ VARIANTS = {
     # are uniform in [512, 1535] (mean ~1023, as the headline workload)
     "dense1b_paged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_paged", page_len=64),
     "dense1b_ragged": WORKLOADS["dense1b_ctx1k"].with_(name="dense1b_ragged", page_len=64, ragged=0.5),
-    # profiling cases: the same models and batches at a short context, so that
-    # a counter capture holds a few GB on the device (weights still exceed L2)
-    "dense24l_b128_ctx256": WORKLOADS["dense24l_b128"].with_(name="dense24l_b128_ctx256", n_prefill=256),
-    "moe64e_top4_ctx256": WORKLOADS["moe64e_top4"].with_(name="moe64e_top4_ctx256", n_prefill=256),
+    # profiling cases: the same models, batches and contexts with two layers,
+    # so that a counter capture holds a few GB on the device (every layer's
+    # kernels have the full-size shapes; weights and caches still exceed L2)
+    "dense24l_b128_2l": WORKLOADS["dense24l_b128"].with_(name="dense24l_b128_2l", n_layers=2),
+    "dense1b_ctx32k_2l": WORKLOADS["dense1b_ctx32k"].with_(name="dense1b_ctx32k_2l", n_layers=2),
+    "moe64e_top4_2l": WORKLOADS["moe64e_top4"].with_(name="moe64e_top4_2l", n_layers=2),
 }
 
 

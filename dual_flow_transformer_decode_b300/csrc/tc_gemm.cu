@@ -596,7 +596,7 @@ __device__ __forceinline__ void fma8(float& acc, const uint4& w, const uint4& x)
 }
 
 __global__ void __launch_bounds__(kGemvThreads, 2)
-    k_gemv(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ X, int K, int nr, EpArgs ep,
+    k_gemv_bf16(const __nv_bfloat16* __restrict__ W, const __nv_bfloat16* __restrict__ X, int K, int nr, EpArgs ep,
            Ctrl* ctrl) {
   __shared__ __align__(16) float st[kGemvRows * kStP];   // [row][kStP] like the tensor-core partial tile
   __shared__ __align__(16) float par[4 * 64];
@@ -954,7 +954,7 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, const
   ep.stall_ns = P.stall_ns;
   if (P.gemv[ep.op]) {
     // a few stacked rows: CUDA-core GEMV, 8 feature pairs per CTA, no split
-    launch_pdl(k_gemv, dim3(tiles_of(n_out) * 8), dim3(kGemvThreads), 0, s,
+    launch_pdl(k_gemv_bf16, dim3(tiles_of(n_out) * 8), dim3(kGemvThreads), 0, s,
                static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(x), K, 2 * P.B, ep, Bf.ctrl);
     return;
   }
