@@ -151,6 +151,11 @@ TEST_CONFIGS = {
     "t_bf16_b128": DFConfig("t_bf16_b128", n_layers=2, d_model=384, n_heads=6, n_kv_heads=2,
                             head_dim=128, ffn_hidden=640, vocab=1000, dtype="bf16",
                             batch=128, n_prefill=12, n_steps=3, gain_std=0.1),
+    # more than 256 stacked rows: the projections take the CUDA-core path,
+    # the attention grid (320 (sequence, KV head) pairs) more than one wave
+    "t_bf16_b160": DFConfig("t_bf16_b160", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
+                            head_dim=128, ffn_hidden=512, vocab=500, dtype="bf16",
+                            batch=160, n_prefill=9, n_steps=2, gain_std=0.1),
     "t_moe": DFConfig("t_moe", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
                       head_dim=128, ffn_hidden=0, vocab=1000, dtype="bf16",
                       batch=5, n_prefill=33, n_steps=5, n_experts=8, top_k=2,

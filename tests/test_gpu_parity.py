@@ -11,8 +11,8 @@ from parity_util import GpuRun, oracle_run, compare_steps, assert_parity, kv_com
 
 pytestmark = pytest.mark.gpu
 
-SMALL = ["t_fp32", "t_fp32_gqa", "t_bf16", "t_bf16_b1", "t_bf16_b9", "t_bf16_long", "t_bf16_b100", "t_bf16_b128", "t_moe",
-         "t_moe_fan"]
+SMALL = ["t_fp32", "t_fp32_gqa", "t_bf16", "t_bf16_b1", "t_bf16_b9", "t_bf16_long", "t_bf16_b100", "t_bf16_b128",
+         "t_bf16_b160", "t_moe", "t_moe_fan"]
 
 
 @pytest.mark.parametrize("name", SMALL)
