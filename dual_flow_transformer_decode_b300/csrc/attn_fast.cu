@@ -258,18 +258,31 @@ __global__ void __launch_bounds__(160, 2)
       if (*abort_flag) break;
       const uint32_t kbase = ptx::smem_u32(ring + st * STAGE);
       const uint32_t vbase = kbase + 2 * BOX;
-      // ---- S[16 rows][16 positions] for positions 16*warp .. +15
-      float sc[2][4];
+      // ---- S[16 rows][16 positions] for positions 16*warp .. +15; dims
+      // 0..63 and 64..127 accumulate separately (four independent MMA
+      // chains instead of two), then add
+      float sc[2][4], sd[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        sd[nt][0] = sd[nt][1] = sd[nt][2] = sd[nt][3] = 0.f;
+      }
       const int kpos = warp * 16 + (mq >> 1) * 8 + r8;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < 4; ++kk) {
         uint32_t b00, b01, b10, b11;  // n-tile 0: (b0, b1), n-tile 1: (b0, b1)
+        uint32_t c00, c01, c10, c11;
         ldsm_x4(kbase + sw_off(kpos, kk * 16 + (mq & 1) * 8), b00, b01, b10, b11);
+        ldsm_x4(kbase + sw_off(kpos, (kk + 4) * 16 + (mq & 1) * 8), c00, c01, c10, c11);
         mma_16816(sc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b00, b01);
         mma_16816(sc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b10, b11);
+        mma_16816(sd[0], qa[kk + 4][0], qa[kk + 4][1], qa[kk + 4][2], qa[kk + 4][3], c00, c01);
+        mma_16816(sd[1], qa[kk + 4][0], qa[kk + 4][1], qa[kk + 4][2], qa[kk + 4][3], c10, c11);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
       // ---- online softmax for rows gq (c0, c1) and gq+8 (c2, c3); with
       // fold, rows gq + 8 hold no query and are skipped
       const int pbase = s0 + it * TP + warp * 16 + 2 * tq;
@@ -289,11 +302,13 @@ __global__ void __launch_bounds__(160, 2)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float mo = m_run[h], mn = fmaxf(mo, mx);
-        corr[h] = (mo == -INFINITY) ? 0.f : expf(mo - mn);
+        // the fast exponential (ex2-based, a few ulp): P enters P·V with
+        // 16 significant bits anyway
+        corr[h] = (mo == -INFINITY) ? 0.f : __expf(mo - mn);
         float sum = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          v[k] = (v[k] == -INFINITY) ? 0.f : expf(v[k] - mn);
+          v[k] = (v[k] == -INFINITY) ? 0.f : __expf(v[k] - mn);
           sum += v[k];
         }
         m_run[h] = mn;

@@ -593,11 +593,14 @@ void launch_attn_combine(const Dims& D, const Buffers& Bf, int splits, const Row
 // logaddexp(log alpha + log p1, log(1 - alpha) + log p2), argmax with the
 // lowest index among equal values ("Mecanismos Clave", Objetivo de Mezcla).
 
+// log(e^x + e^y) with the fast exponential and logarithm: log(1 + e) for
+// e = e^(mn - mx) in (0, 1], absolute error a few 1e-7 -- far below the
+// bf16-driven deviations of the log-probabilities it produces.
 __device__ __forceinline__ float logaddexp_f(float x, float y) {
   if (x == -INFINITY) return y;
   if (y == -INFINITY) return x;
   float mx = fmaxf(x, y), mn = fminf(x, y);
-  return mx + log1pf(expf(mn - mx));
+  return mx + __logf(1.0f + __expf(mn - mx));
 }
 
 // One cluster of kMixCl CTAs per sequence; CTA r handles the r-th chunk of
@@ -623,7 +626,7 @@ __device__ __forceinline__ void mix_merge(float& m, float& s, float& q, float mo
     return;
   }
   const float mn = fmaxf(m, mo);
-  const float ea = expf(m - mn), eb = expf(mo - mn);
+  const float ea = __expf(m - mn), eb = __expf(mo - mn);
   s = s * ea + so * eb;
   q = q * ea * ea + qo * eb * eb;
   m = mn;
@@ -635,14 +638,17 @@ __device__ __forceinline__ void mix_merge(MixStat& a, const MixStat& o) {
   mix_merge(a.m2, a.s2, dummy, o.m2, o.s2, 0.f);
 }
 
+// Online softmax statistics: running max m, sum of e^(x - m) and of
+// e^(2(x - m)).  The fast exponential (ex2-based, a few ulp) suffices: the
+// sums feed log-probabilities compared at the bf16 level.
 __device__ __forceinline__ void mix_push(float& m, float& s, float& q, float x) {
   if (x > m) {
-    const float r = expf(m - x);
+    const float r = __expf(m - x);
     s = s * r + 1.f;
     q = q * r * r + 1.f;
     m = x;
   } else {
-    const float e = expf(x - m);
+    const float e = __expf(x - m);
     s += e;
     q += e * e;
   }
