@@ -330,12 +330,16 @@ __global__ void __launch_bounds__(160, 2)
         // At most 8 query rows: the lo part of row gq takes the MMA's
         // otherwise idle row gq + 8, so one MMA applies both parts (rows
         // gq + 8 accumulate lo * V; they are added to rows gq at the end).
+        // Once the running maxima settle every factor is 1 and the rescale
+        // (exact either way) is skipped.
+        if (__any_sync(0xffffffffu, corr[0] != 1.f)) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          o[j][0] *= corr[0];
-          o[j][1] *= corr[0];
-          o[j][2] *= corr[0];
-          o[j][3] *= corr[0];
+          for (int j = 0; j < 16; ++j) {
+            o[j][0] *= corr[0];
+            o[j][1] *= corr[0];
+            o[j][2] *= corr[0];
+            o[j][3] *= corr[0];
+          }
         }
         // ---- O += P V: V^T fragments by ldmatrix.trans, two 8-dim n-tiles per load
 #pragma unroll
@@ -529,7 +533,7 @@ bool attn_fast_init(AttnPlan& P, const Dims& D, void* kv, std::string* err) {
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(sp, 1, 1);
     lc.blockDim = dim3(160);
-    lc.dynamicSmemBytes = smem_bytes(kLongStages);
+    lc.dynamicSmemBytes = smem_bytes(kShortStages);  // split launches use the short ring
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = sp;
@@ -584,15 +588,16 @@ void attn_fast(const AttnPlan& P, const Dims& D, const Buffers& Bf, const void* 
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(splits, D.Hkv, R.B);
   lc.blockDim = dim3(160);
-  // Ring depth from the tiles a split streams (over the context capacity,
-  // so one captured launch serves every position): three 32 KB stages when
-  // a split has at least kLongTiles tiles (measured, 4096 positions at
-  // batch 128: 173.6 -> 166.5 us; 32768 positions: 52.9 -> 48.1 us), two
-  // for short splits (1023 positions in 4 splits: 13.0 against 13.2 us);
-  // both let two attention CTAs share an SM.  L2 prefetch of the split
-  // measured no faster.
+  // Ring depth: three 32 KB stages for an unsplit launch whose CTAs stream
+  // at least kLongTiles tiles (over the context capacity, so one captured
+  // launch serves every position), else two.  Measured inside the whole
+  // step: batch 128 at 4096 positions 6.040 -> 6.014 ms per step with three;
+  // at 32768 positions in 12-CTA clusters three stages were 47 against 53 us
+  // per launch alone but 2.045 against 1.604 ms per step, because the larger
+  // clusters then wait for the neighbouring kernels' resident CTAs to leave.
+  // L2 prefetch of the split measured no faster.
   const int tiles_per_split = ((D.max_len + TP - 1) / TP + splits - 1) / splits;
-  const int ns = tiles_per_split >= kLongTiles ? kLongStages : kShortStages, l2pf = 0;
+  const int ns = (splits == 1 && tiles_per_split >= kLongTiles) ? kLongStages : kShortStages, l2pf = 0;
   lc.dynamicSmemBytes = smem_bytes(ns);
   lc.stream = s;
   cudaLaunchAttribute at[2];
