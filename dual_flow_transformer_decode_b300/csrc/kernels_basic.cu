@@ -151,13 +151,21 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a,
 template <typename T>
 __global__ void k_rmsnorm(const float* __restrict__ h, const float* __restrict__ g, T* __restrict__ out,
                           float* __restrict__ out_f32, int d, float eps, int lo) {
-  ptx::grid_dep_wait();
-  ptx::grid_dep_launch();
   __shared__ float red[32];
   const int m = lo + blockIdx.x;
   const float4* x4 = reinterpret_cast<const float4*>(h + (size_t)m * d);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   const int n4 = d >> 2;
+  // the gains are fixed inputs: read before the dependency resolves, so only
+  // the row load and the reduction sit on the critical path
+  float4 gv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = threadIdx.x + k * 256;
+    if (i < n4) gv[k] = g4[i];
+  }
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   float4 v[8];
   float ss = 0.f;
 #pragma unroll
@@ -174,7 +182,7 @@ __global__ void k_rmsnorm(const float* __restrict__ h, const float* __restrict__
   for (int k = 0; k < 8; ++k) {
     const int i = threadIdx.x + k * 256;
     if (i < n4) {
-      const float4 gg = g4[i];
+      const float4 gg = gv[k];
       const float a = v[k].x * r * gg.x, b = v[k].y * r * gg.y, c = v[k].z * r * gg.z, e = v[k].w * r * gg.w;
       store4<T>(out + (size_t)m * d + 4 * i, a, b, c, e);
       if (out_f32) *reinterpret_cast<float4*>(out_f32 + (size_t)m * d + 4 * i) = make_float4(a, b, c, e);

@@ -759,11 +759,15 @@ int choose_splits(int n_out, int K, int sms, int per_sm) {
 // for this kernel and footprint, less two clusters of headroom for the
 // neighbouring kernels' CTAs that programmatic dependent launch keeps
 // resident) would run in two waves.  The largest split count up to 8 that
-// still gives each split at least two K blocks and fits one wave is taken.
+// still gives each split at least eight K blocks and fits one wave is
+// taken.  (Measured at 256 rows, six layers of dense24l_b128: QKV and Wo
+// with K = 2048 took 13.4 / 12.9 us per launch at 5 / 6 splits and 12.5 /
+// 12.2 us at 4, the step 1.556 -> 1.528 ms for Wo alone; down with K = 8192
+// was fastest at 6 splits.)
 int choose_splits_wide(int n_out, int K, int sms, const int* max_clusters) {
   const int tiles = tiles_of(n_out), kb = K / kBK;
   for (int s = 8; s > 1; --s) {
-    if (kb / s < 2 || tiles * s > sms) continue;
+    if (kb / s < 8 || tiles * s > sms) continue;
     if (tiles <= max_clusters[s] - 2) return s;
   }
   return 1;
