@@ -144,10 +144,12 @@ TEST_CONFIGS = {
                           batch=1, n_prefill=70, n_steps=5, gain_std=0.1),
     # more than 128 stacked rows: the tensor-core GEMMs take their wide form
     # (one tile of up to 256 stacked rows per SM); 100 sequences give 200
-    # rows (padded to 208), no K-split at this width; 128 give exactly 256,
-    # and d_model 1024 gives two K-splits reduced through L2
+    # rows (padded to 208), no K-split at this width, and a vocabulary of
+    # more 128-row tiles than SMs (an LM head written straight from TMEM,
+    # last tile ragged); 128 give exactly 256, and d_model 1024 gives two
+    # K-splits reduced through L2
     "t_bf16_b100": DFConfig("t_bf16_b100", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2,
-                            head_dim=128, ffn_hidden=512, vocab=700, dtype="bf16",
+                            head_dim=128, ffn_hidden=512, vocab=20100, dtype="bf16",
                             batch=100, n_prefill=20, n_steps=3, gain_std=0.1),
     "t_bf16_b128": DFConfig("t_bf16_b128", n_layers=2, d_model=1024, n_heads=8, n_kv_heads=2,
                             head_dim=128, ffn_hidden=1024, vocab=1000, dtype="bf16",

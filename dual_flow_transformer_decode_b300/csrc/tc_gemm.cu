@@ -393,7 +393,7 @@ __device__ __forceinline__ void epilogue(const EpArgs& ep, cg::cluster_group& cl
 // form a thread-block cluster (cluster rank = split index).  NT threads:
 // warp 0 TMA producer, warp 1 MMA issuer, all of them drain TMEM and run the
 // epilogue (256 when the footprint allows one CTA per SM anyway: wide N).
-template <int NT>
+template <int NT, bool DIRECT = false>
 __global__ void __launch_bounds__(NT, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, int N, int kblocks,
               int kStages, EpArgs ep, Ctrl* ctrl) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(NT, 1)
   // the epilogue's partial tile [N][128] fp32 reuses the ring; the region is
   // the larger of the two
   size_t region = (size_t)kStages * (kStageW + stage_x);
-  if ((size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;
+  if (!DIRECT && (size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;
   float* par = reinterpret_cast<float*>(base + region);  // [4][64] epilogue parameters
   uint64_t* full = reinterpret_cast<uint64_t*>(par + 4 * 64);
   uint64_t* empty = full + kMaxStages;
@@ -520,6 +520,31 @@ __global__ void __launch_bounds__(NT, 1)
   }
   __syncthreads();
   const bool aborted = flags[0] != 0;
+
+  if constexpr (DIRECT) {
+    // LOGITS from TMEM: lane r of a warp's quarter holds vocabulary entry
+    // n0 + 32 (w % 4) + r for the stacked rows of each column chunk; a
+    // warp's store of one row is 32 consecutive floats
+    ptx::grid_dep_launch();
+    if (!aborted) {
+      const int quarter = warp & 3, r = quarter * 32 + lane, gv = tile * kBM + r;
+      const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+      const bool ok_v = gv < ep.n_out;
+      for (int j0 = (warp >> 2) * 16; j0 < N; j0 += 16 * (NT / 128)) {
+        float v[16];
+        ptx::tmem_ld16(trow + j0, v);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int m = j0 + q;
+          if (ok_v && m >= ep.lo && m < ep.hi) ep.logits[(size_t)m * ep.V + gv] = v[q];
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, ncols);
+    return;
+  }
 
   if (!aborted) {
     // TMEM -> partial tile st[column j][weight row r]; warp w reads TMEM
@@ -781,9 +806,9 @@ int stages_for(int N, int kb = 64) {
   return st;
 }
 
-size_t smem_bytes(int N, int stages) {
+size_t smem_bytes(int N, int stages, bool direct = false) {
   size_t region = (size_t)stages * (kStageW + N * kBK * 2);
-  if ((size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;  // epilogue partial tile
+  if (!direct && (size_t)N * kStP * 4 > region) region = (size_t)N * kStP * 4;  // epilogue partial tile
   return region + 1024 + 4 * 64 * 4 + 256;
 }
 
@@ -849,6 +874,7 @@ bool tc_plan_init(TcPlan& P, const Dims& D, const Buffers& Bf, const std::vector
   cudaFuncSetAttribute(k_tc_gemm<256>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   cudaFuncSetAttribute(k_tc_gemm<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   cudaFuncSetAttribute(k_tc_gemm<512>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncSetAttribute(k_tc_gemm<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   P.enabled = true;
   P.dense = !D.E;
   return true;
@@ -967,10 +993,15 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, const
   lc.blockDim = dim3(128);
   // ~64 KB rings let two GEMM CTAs and a neighbouring kernel's CTA share an
   // SM; a launch of at most one CTA per SM may use a deeper ring, and a wide
-  // tile (its partial tile alone takes half the SM) the deepest.
+  // tile (its partial tile alone takes half the SM) the deepest.  The LM
+  // head of a wide batch has more tiles than SMs and no K-split: its logits
+  // leave straight from TMEM, and a two-stage ring lets two CTAs share an SM
+  // so that the launch runs in one wave instead of two.
+  const bool direct = ep.op == (int)TcOp::LOGITS && splits == 1 && P.npad > kWideN && tiles_of(n_out) > P.sms;
   const bool one_per_sm = tiles_of(n_out) * splits <= P.sms;
-  const int stages = stages_for(P.npad, P.npad > kWideN ? kWideKB : one_per_sm ? DF_GEMM_WIDE_KB : 64);
-  lc.dynamicSmemBytes = smem_bytes(P.npad, stages);
+  const int stages =
+      direct ? 2 : stages_for(P.npad, P.npad > kWideN ? kWideKB : one_per_sm ? DF_GEMM_WIDE_KB : 64);
+  lc.dynamicSmemBytes = smem_bytes(P.npad, stages, direct);
   lc.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -983,7 +1014,10 @@ void launch(const TcPlan& P, const CUtensorMap& tw, const CUtensorMap& tx, const
   lc.numAttrs = 2;
   // a footprint above half the SM already means one CTA per SM: use the
   // wider CTA, whose extra warps share the epilogue
-  if (P.npad > kWideN) {
+  if (direct) {
+    // LOGITS straight from TMEM (k_tc_gemm<128, true>): no partial tile
+    cudaLaunchKernelEx(&lc, k_tc_gemm<128, true>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
+  } else if (P.npad > kWideN) {
     // 256 stacked rows: 16 warps share the TMEM drain and the epilogue
     lc.blockDim = dim3(512);
     cudaLaunchKernelEx(&lc, k_tc_gemm<512>, tw, tx, P.npad, K / kBK, stages, ep, Bf.ctrl);
