@@ -27,7 +27,13 @@ namespace df {
 
 namespace {
 
-constexpr int kStages = 4;
+// Ring depth.  Two stages (about 50 KB of shared memory at 64 stacked rows,
+// four CTAs per SM) measured faster than four stages at two CTAs per SM:
+// the MoE step 3.26 -> 3.21 ms, with the auxiliary fan-out 3.65 -> 3.49 ms;
+// one stage (six CTAs per SM, no overlap inside a CTA) 3.84 ms.  The
+// weight stream of one CTA is bound by its own load -> MMA -> release
+// round trips, so more CTAs per SM stream more than deeper rings.
+constexpr int kStages = 2;
 constexpr int kBK = 64;
 constexpr int kBM = 128;
 constexpr int kStageW = kBM * kBK * 2;
@@ -47,25 +53,31 @@ struct MoeArgs {
   int op;         // 0: gate/up, 1: down
   int tiles;      // 128-row weight tiles per expert
   int rows_w;     // weight rows per expert (2Fe or d)
+  int stages;     // ring depth
 };
 
 __global__ void __launch_bounds__(128, 1)
     k_tc_moe(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx, int K, MoeArgs a) {
   const int e = blockIdx.x / a.tiles, tile = blockIdx.x % a.tiles;
-  ptx::grid_dep_wait();
-  const int cnt = a.ecount[e];
+  // Routing finished before the previous kernel's CTAs passed their own
+  // dependency wait, which each of them does before it lets this grid
+  // start, so the expert's entry count is final here (read from L2, not
+  // through L1): CTAs of unselected experts leave at once and the others
+  // request their first weight stages before the dependency resolves.
+  const int cnt = __ldcg(a.ecount + e);
   if (cnt == 0) return;  // uniform across the CTA
+  const int S = a.stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = (2 * cnt + 15) / 16 * 16;
   const int stage_x = N * kBK * 2;
   uint8_t* sw = base;
-  uint8_t* sx = base + kStages * kStageW;
-  size_t region = (size_t)kStages * (kStageW + (size_t)a.nxe * kBK * 2);
+  uint8_t* sx = base + S * kStageW;
+  size_t region = (size_t)S * (kStageW + (size_t)a.nxe * kBK * 2);
   if ((size_t)a.nxe * kBM * 4 > region) region = (size_t)a.nxe * kBM * 4;
   uint64_t* full = reinterpret_cast<uint64_t*>(base + region);
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  uint64_t* empty = full + S;
+  uint64_t* done = empty + S;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tslot + 1);
   float* st = reinterpret_cast<float*>(base);  // [N][128] result tile, reuses the ring
@@ -78,7 +90,7 @@ __global__ void __launch_bounds__(128, 1)
   if (tid == 0) {
     ptx::prefetch_tmap(&tw);
     ptx::prefetch_tmap(&tx);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -99,9 +111,20 @@ __global__ void __launch_bounds__(128, 1)
 
   if (warp == 0 && lane == 0) {
     const uint64_t pol_w = ptx::policy_evict_first();
-    for (int i = 0; i < nk; ++i) {
-      const int s = i % kStages;
-      if (i >= kStages && !ptx::mbar_wait(&empty[s], ((i / kStages) - 1) & 1)) {
+    // the weights do not depend on the previous kernel: the first stages'
+    // weight tiles are requested before waiting for it
+    const int pre = nk < S ? nk : S;
+    for (int i = 0; i < pre; ++i) {
+      ptx::mbar_arrive_expect_tx(&full[i], kStageW + stage_x);
+      ptx::tma_load_2d_hint(sw + i * kStageW, &tw, &full[i], i * kBK, wrow, pol_w);
+    }
+    ptx::grid_dep_wait();
+    for (int i = 0; i < pre; ++i)
+      for (int q = 0; q < N / kXBox; ++q)
+        ptx::tma_load_2d(sx + i * stage_x + q * kXBox * kBK * 2, &tx, &full[i], i * kBK, xrow + q * kXBox);
+    for (int i = pre; i < nk; ++i) {
+      const int s = i % S;
+      if (!ptx::mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
         flags[0] = 1;
         latch_error(a.ctrl, kErrTimeout, 300);
         break;
@@ -114,8 +137,8 @@ __global__ void __launch_bounds__(128, 1)
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = ptx::idesc_bf16_f32(kBM, N);
     for (int i = 0; i < nk; ++i) {
-      const int s = i % kStages;
-      if (!ptx::mbar_wait(&full[s], (i / kStages) & 1)) {
+      const int s = i % S;
+      if (!ptx::mbar_wait(&full[s], (i / S) & 1)) {
         flags[0] = 1;
         latch_error(a.ctrl, kErrTimeout, 301);
         break;
@@ -129,6 +152,8 @@ __global__ void __launch_bounds__(128, 1)
       ptx::mma_commit(&empty[s]);
     }
     ptx::mma_commit(done);
+  } else {
+    ptx::grid_dep_wait();
   }
   __syncwarp();
   const bool ok = ptx::mbar_wait(done, 0);
@@ -283,10 +308,10 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int nxe) {
-  size_t region = (size_t)kStages * (kStageW + (size_t)nxe * kBK * 2);
+size_t smem_bytes(int nxe, int stages) {
+  size_t region = (size_t)stages * (kStageW + (size_t)nxe * kBK * 2);
   if ((size_t)nxe * kBM * 4 > region) region = (size_t)nxe * kBM * 4;
-  return 1024 + region + 2 * kStages * 8 + 8 + 16;
+  return 1024 + region + 2 * (size_t)stages * 8 + 8 + 16;
 }
 
 }  // namespace
@@ -300,8 +325,10 @@ bool moe_tc_init(MoePlan& P, const Dims& D, const Buffers& Bf, const std::vector
   if (e && e[0] == '1') return true;
   if (!D.E || !D.bf16 || D.d % kBM || D.Fe % kBK) return true;  // gate/up tiles: Fe/64 (64 gate + 64 up rows)
   const int nxe = moe_nxe(D);
-  if (nxe > 256 || smem_bytes(nxe) > 227 * 1024) return true;
+  const int st = kStages;
+  if (nxe > 256 || smem_bytes(nxe, st) > 227 * 1024) return true;
   P.nxe = nxe;
+  P.stages = st;
   P.w_gu.resize(D.L);
   P.w_d.resize(D.L);
   bool ok = true;
@@ -315,7 +342,7 @@ bool moe_tc_init(MoePlan& P, const Dims& D, const Buffers& Bf, const std::vector
     if (err) *err = "cuTensorMapEncodeTiled failed for an expert matrix";
     return false;
   }
-  cudaFuncSetAttribute(k_tc_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(nxe));
+  cudaFuncSetAttribute(k_tc_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(nxe, kStages));
   P.enabled = true;
   return true;
 }
@@ -351,11 +378,14 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
   a.op = 0;
   a.tiles = 2 * D.Fe / kBM;
   a.rows_w = 2 * D.Fe;
-  launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe), s, P.w_gu[layer], P.x_g, D.d, a);
+  a.stages = P.stages;
+  launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe, P.stages), s, P.w_gu[layer], P.x_g, D.d,
+             a);
   a.op = 1;
   a.tiles = D.d / kBM;
   a.rows_w = D.d;
-  launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe), s, P.w_d[layer], P.x_z, D.Fe, a);
+  launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe, P.stages), s, P.w_d[layer], P.x_z, D.Fe,
+             a);
   const int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
   launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt,
              (const float*)Bf.gate, topk_l, (const int*)Bf.topkx, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo,

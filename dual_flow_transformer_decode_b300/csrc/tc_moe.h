@@ -11,7 +11,8 @@ namespace df {
 
 struct MoePlan {
   bool enabled = false;
-  int nxe = 0;  // rows of one expert's packed block: 2 * max_batch padded to 16
+  int nxe = 0;     // rows of one expert's packed block: 2 * max_batch padded to 16
+  int stages = 0;  // TMA ring depth of the expert GEMMs
   std::vector<CUtensorMap> w_gu, w_d;
   CUtensorMap x_g, x_z;
 };
