@@ -74,7 +74,6 @@ struct Buffers {
   float* q1s;       // [L][maxB][qdim] saved primary pre-RoPE queries (ungrouped)
   float* z1s;       // [L][maxB][F] (MoE: [L][maxB][k][Fe]) saved primary MLP hidden
   float* y1s;       // [L][maxB][d] saved primary MLP output
-  float* rlog;      // [2maxB][E] router logits
   int* topk;        // [L][maxB][k] primary expert sets
   float* gate;      // [2maxB][ka] gate weights per row (primary rows use the first k)
   int* topkx;       // [maxB][ka-k] this layer's auxiliary-own experts
@@ -83,6 +82,7 @@ struct Buffers {
   void* zE;         // [2][maxB][ka][Fe] expert hidden (dtype)
   float* yE;        // [2][maxB][ka][d] expert outputs fp32
   int* eslot;       // [maxB*ka] position of each entry in its expert's list
+  int* ticket;      // [1] arrivals at the routing launch (the last CTA builds the entry lists and resets it)
   void* xg;         // [E][nxe][d] packed expert input rows (tensor-core MoE path)
   void* zEt;        // [E][nxe][Fe] packed expert hidden rows
   float* yEt;       // [E][nxe][d] packed expert outputs
@@ -172,9 +172,11 @@ void launch_mix(const Dims& D, const Buffers& Bf, int B, int aux_on, float* logp
                 cudaStream_t s);
 
 // MoE with router replay.
-void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s);
-void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R,
-                      int32_t* dbg_topk, float* dbg_router, cudaStream_t s);
+// Router logits of rows R and routing (top-k of the primary rows when
+// `select`, else the saved choice; gates of both flows; per-expert entry
+// lists) in one launch.
+void launch_router_route(const Dims& D, const Buffers& Bf, const void* Wr, int layer, int select, const Rows& R,
+                         int32_t* dbg_topk, float* dbg_router, cudaStream_t s);
 void launch_moe_gateup_generic(const Dims& D, const Buffers& Bf, const void* wgu, const float* bvec,
                                const Couple& C, const Rows& R, cudaStream_t s);
 void launch_moe_down_generic(const Dims& D, const Buffers& Bf, const void* wd, const Rows& R,

@@ -242,7 +242,6 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.q1s = (float*)take((size_t)D.L * D.maxB * D.qdim * 4);
   b.z1s = (float*)take((size_t)D.L * D.maxB * zs * 4);
   b.y1s = (float*)take((size_t)D.L * D.maxB * D.d * 4);
-  b.rlog = (float*)take(D.E ? M2 * D.E * 4 : 0);
   b.topk = (int*)take(D.E ? (size_t)D.L * D.maxB * D.k * 4 : 0);
   b.gate = (float*)take(D.E ? M2 * D.ka * 4 : 0);
   b.topkx = (int*)take(D.E ? (size_t)D.maxB * (D.ka - D.k) * 4 : 0);
@@ -251,6 +250,7 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.zE = take(D.E ? 2 * (size_t)D.maxB * D.ka * D.Fe * esz : 0);
   b.yE = (float*)take(D.E ? 2 * (size_t)D.maxB * D.ka * D.d * 4 : 0);
   b.eslot = (int*)take(D.E ? (size_t)D.maxB * D.ka * 4 : 0);
+  b.ticket = (int*)take(D.E ? 16 : 0);
   const size_t nxe = D.E ? (size_t)df::moe_nxe(D) : 0;
   b.xg = take(D.E * nxe * D.d * esz);
   b.zEt = take(D.E * nxe * D.Fe * esz);
@@ -353,8 +353,7 @@ void op_moe(df_ctx* X, int l, const Rows& R, const Couple& C) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
-  df::launch_router(D, Bf, X->router[l], R, s);
-  df::launch_moe_route(D, Bf, l, R.has_primary() ? 1 : 0, R, X->dbg_topk, X->dbg_router, s);
+  df::launch_router_route(D, Bf, X->router[l], l, R.has_primary() ? 1 : 0, R, X->dbg_topk, X->dbg_router, s);
   if (!X->force_generic && X->moe.enabled) {
     df::moe_tc_forward(X->moe, D, Bf, l, X->b[l], X->c[l], C, R, s);
   } else {

@@ -8,6 +8,7 @@
 // sections "Arquitectura Central" and "Mecanismos Clave".  Stacked rows:
 // 0..B-1 primary flow, B..2B-1 auxiliary flow (same sequence order).
 
+#include <algorithm>
 #include <math.h>
 #include <stdlib.h>
 
@@ -74,6 +75,12 @@ constexpr int kRouterRows = 4;  // stacked rows per router CTA
 template <typename TW, int R>
 __global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const float* __restrict__ un,
                                                 float* __restrict__ rlog, int E, int d, int lo, int hi);
+template <typename TW>
+__global__ void __launch_bounds__(512, 2) k_router_route(
+    const TW* __restrict__ Wr, const float* __restrict__ un, int* __restrict__ topk_l, int* __restrict__ topkx,
+    float* __restrict__ gate, int* __restrict__ ecount, int* __restrict__ elist, int* __restrict__ eslot,
+    int* __restrict__ ticket, int B, int E, int d, int k, int ka, int maxB, int select, int prim, int aux,
+    int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l);
 
 void kernels_init() {
   cudaFuncSetAttribute(k_attn_generic<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -82,6 +89,9 @@ void kernels_init() {
                        kRouterRows * 8192 * 4);
   cudaFuncSetAttribute(k_router<float, kRouterRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        kRouterRows * 8192 * 4);
+  cudaFuncSetAttribute(k_router_route<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (2 * 8192 + 2 * 1024) * 4);
+  cudaFuncSetAttribute(k_router_route<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (2 * 8192 + 2 * 1024) * 4);
 }
 
 void launch_set_pos(Ctrl* c, int t, cudaStream_t s) { launch_pdl(k_set_pos, dim3(1), dim3(1), 0, s, c, t); }
@@ -906,19 +916,6 @@ __global__ void __launch_bounds__(256) k_router(const TW* __restrict__ Wr, const
   }
 }
 
-void launch_router(const Dims& D, const Buffers& Bf, const void* Wr, const Rows& R, cudaStream_t s) {
-  const int n = R.hi - R.lo;
-  if (n <= 0) return;
-  const dim3 grid((n + kRouterRows - 1) / kRouterRows, (D.E + 7) / 8);
-  const size_t smem = (size_t)kRouterRows * D.d * sizeof(float);  // d <= 8192: at most 128 KB
-  if (D.bf16)
-    launch_pdl(k_router<__nv_bfloat16, kRouterRows>, grid, dim3(256), smem, s, (const __nv_bfloat16*)Wr,
-               (const float*)Bf.un, Bf.rlog, D.E, D.d, R.lo, R.hi);
-  else
-    launch_pdl(k_router<float, kRouterRows>, grid, dim3(256), smem, s, (const float*)Wr, (const float*)Bf.un,
-               Bf.rlog, D.E, D.d, R.lo, R.hi);
-}
-
 void launch_router_rows(const Dims& D, const void* Wr, const float* un, float* rlog, int rows, cudaStream_t s) {
   if (rows <= 0) return;
   const dim3 grid((rows + kRouterRows - 1) / kRouterRows, (D.E + 7) / 8);
@@ -991,32 +988,114 @@ __device__ __forceinline__ float entry_gate(float v, int n, int lane) {
   return ex / den;
 }
 
-__global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ topk_l, int* __restrict__ topkx,
-                            float* __restrict__ gate, int* __restrict__ ecount, int* __restrict__ elist,
-                            int* __restrict__ eslot, int B, int E, int k, int ka, int maxB, int select, int prim,
-                            int aux, int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l, int stage) {
+
+// Router logits and routing in one launch.  A cluster of kRouteCl CTAs
+// serves sequence b: CTA r computes the router logits of the sequence's
+// active rows (primary b, auxiliary B + b) for its share of the experts,
+// with the same per-(row, expert) arithmetic as k_router; rank 0 gathers the
+// logits through distributed shared memory and routes the sequence as
+// described above.  The last rank-0 CTA to finish (a ticket counter in
+// global memory, reset by that CTA) builds the per-expert entry lists from
+// every sequence's selection.
+constexpr int kRouteThreads = 512;
+constexpr int kRouteCl = 4;     // CTAs per sequence (cluster)
+constexpr int kRouteBatch = 8;  // 16-byte weight loads of one lane in flight at once
+
+template <typename TW>
+__global__ void __launch_bounds__(kRouteThreads, 2) k_router_route(
+    const TW* __restrict__ Wr, const float* __restrict__ un, int* __restrict__ topk_l, int* __restrict__ topkx,
+    float* __restrict__ gate, int* __restrict__ ecount, int* __restrict__ elist, int* __restrict__ eslot,
+    int* __restrict__ ticket, int B, int E, int d, int k, int ka, int maxB, int select, int prim, int aux,
+    int32_t* __restrict__ dbg_topk_l, float* __restrict__ dbg_router_l) {
+  // [2][d] the sequence's rows (primary, auxiliary), then (last CTA) the
+  // entries; [2][E] router logits (this CTA's experts; rank 0: all)
+  extern __shared__ float rsm_raw[];
+  float* xr = rsm_raw;
+  float* rsm = rsm_raw + 2 * d;
+  __shared__ int last;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  const int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cl.block_rank(), b = blockIdx.y;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = kRouteThreads / 32;
   const int kx = aux ? ka - k : 0;  // auxiliary-own experts per token
-  // The router rows of the active flows are read once into shared memory
-  // when they fit (the selection rounds re-read them), else from global.
-  extern __shared__ float rsm[];  // [2B][E] when staged
-  const float* rl = rlog;
-  if (stage) {
-    const int lo = prim ? 0 : B, hi = aux ? 2 * B : B;
-    for (int i = lo * E + (int)threadIdx.x; i < hi * E; i += blockDim.x) rsm[i] = rlog[i];
-    __syncthreads();
-    rl = rsm;
+  const int per = (E + kRouteCl - 1) / kRouteCl, e0 = rank * per, e1 = min(E, e0 + per);
+  {
+    const int n4 = d / 4;
+    const float4* s0 = reinterpret_cast<const float4*>(un + (size_t)b * d);
+    const float4* s1 = reinterpret_cast<const float4*>(un + (size_t)(B + b) * d);
+    float4* d4 = reinterpret_cast<float4*>(xr);
+    for (int i = threadIdx.x; i < n4; i += kRouteThreads) {
+      if (prim) d4[i] = s0[i];
+      if (aux) d4[n4 + i] = s1[i];
+    }
   }
-  // one warp per sequence
-  for (int b = w; b < B; b += warps) {
+  __syncthreads();
+  // ---- logits of experts e0 + w, e0 + w + 16, ... for both rows, with
+  // kRouteBatch weight loads per lane in flight
+  constexpr int VEC = 16 / sizeof(TW);
+  for (int e = e0 + w; e < e1; e += warps) {
+    const TW* wr = Wr + (size_t)e * d;
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int c0 = 0; c0 < d; c0 += 32 * VEC * kRouteBatch) {
+      uint4 raw[kRouteBatch];
+#pragma unroll
+      for (int t = 0; t < kRouteBatch; ++t) {
+        const int k0 = c0 + (t * 32 + lane) * VEC;
+        if (k0 < d) raw[t] = *reinterpret_cast<const uint4*>(wr + k0);
+      }
+#pragma unroll
+      for (int t = 0; t < kRouteBatch; ++t) {
+        const int k0 = c0 + (t * 32 + lane) * VEC;
+        if (k0 >= d) break;
+        const TW* wv = reinterpret_cast<const TW*>(&raw[t]);
+        if (prim) {
+#pragma unroll
+          for (int q4 = 0; q4 < VEC / 4; ++q4) {
+            const float4 x = *reinterpret_cast<const float4*>(xr + k0 + 4 * q4);
+            acc0 = fmaf(Num<TW>::to_f(wv[4 * q4]), x.x, acc0);
+            acc0 = fmaf(Num<TW>::to_f(wv[4 * q4 + 1]), x.y, acc0);
+            acc0 = fmaf(Num<TW>::to_f(wv[4 * q4 + 2]), x.z, acc0);
+            acc0 = fmaf(Num<TW>::to_f(wv[4 * q4 + 3]), x.w, acc0);
+          }
+        }
+        if (aux) {
+#pragma unroll
+          for (int q4 = 0; q4 < VEC / 4; ++q4) {
+            const float4 x = *reinterpret_cast<const float4*>(xr + d + k0 + 4 * q4);
+            acc1 = fmaf(Num<TW>::to_f(wv[4 * q4]), x.x, acc1);
+            acc1 = fmaf(Num<TW>::to_f(wv[4 * q4 + 1]), x.y, acc1);
+            acc1 = fmaf(Num<TW>::to_f(wv[4 * q4 + 2]), x.z, acc1);
+            acc1 = fmaf(Num<TW>::to_f(wv[4 * q4 + 3]), x.w, acc1);
+          }
+        }
+      }
+    }
+    acc0 = warp_sum(acc0);
+    acc1 = warp_sum(acc1);
+    if (lane == 0) {
+      rsm[e] = acc0;
+      rsm[E + e] = acc1;
+    }
+  }
+  cl.sync();
+  if (rank == 0) {
+    for (int i = threadIdx.x; i < 2 * E; i += kRouteThreads) {
+      const int e = i < E ? i : i - E, owner = e / per;
+      if (owner != 0) rsm[i] = cl.map_shared_rank(rsm, owner)[i];
+    }
+  }
+  // the other ranks' logits stay readable until rank 0 has copied them
+  cl.sync();
+  if (rank != 0) return;
+  // ---- routing of sequence b (warp 0 of rank 0)
+  if (w == 0) {
     int sel = 0;  // lane j < k: the j-th replayed expert
-    unsigned long long tlo = 0ull, thi = 0ull;  // experts 0..63 and 64..127 of each lane's stride
+    unsigned long long tlo = 0ull, thi = 0ull;
     if (select) {
-      const float* r = rl + (size_t)b * E;
       for (int j = 0; j < k; ++j) {
-        const int bi = warp_pick(r, E, lane, tlo, thi);
+        const int bi = warp_pick(rsm, E, lane, tlo, thi);
         if (lane == 0) topk_l[b * k + j] = bi;
         if (lane == j) sel = bi;
         mark_taken(bi, lane, tlo, thi);
@@ -1025,16 +1104,13 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
       if (lane < k) sel = topk_l[b * k + lane];
       for (int j = 0; j < k; ++j) mark_taken(__shfl_sync(0xffffffffu, sel, j), lane, tlo, thi);
     }
-    // primary gates over the replayed set
     if (prim) {
-      const float* r = rl + (size_t)b * E;
-      const float g = entry_gate(lane < k ? r[sel] : -INFINITY, k, lane);
+      const float g = entry_gate(lane < k ? rsm[sel] : -INFINITY, k, lane);
       if (lane < k) gate[(size_t)b * ka + lane] = g;
     }
-    // auxiliary: its own experts outside the replayed set, gates over the union
     int own = 0;  // lane k + j: the j-th auxiliary-own expert
     if (aux) {
-      const float* r = rl + (size_t)(B + b) * E;
+      const float* r = rsm + E;
       for (int j = 0; j < kx; ++j) {
         const int bi = warp_pick(r, E, lane, tlo, thi);
         if (lane == 0) topkx[b * kx + j] = bi;
@@ -1048,16 +1124,30 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
     }
     if (dbg_topk_l && prim && lane < k) dbg_topk_l[b * ka + lane] = sel;
     if (dbg_router_l && prim)
-      for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rl[(size_t)b * E + e];
+      for (int e = lane; e < E; e += 32) dbg_router_l[(size_t)b * E + e] = rsm[e];
+    // this sequence's selection is visible device-wide before the ticket
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) last = atomicAdd(ticket, 1) == (int)gridDim.y - 1;  // one arrival per sequence
   }
   __syncthreads();
-  // entry lists in ascending entry order: warp per expert, 32 entries a round
+  if (!last) return;
+  // ---- the last CTA: entry lists in ascending entry order, warp per expert
+  __threadfence();
+  if (threadIdx.x == 0) *ticket = 0;
   const int nent = B * k + B * kx;
+  const bool staged = nent <= 2 * d;
+  int* ents = reinterpret_cast<int*>(xr);
+  if (staged) {
+    for (int i = threadIdx.x; i < nent; i += kRouteThreads)
+      ents[i] = i < B * k ? __ldcg(topk_l + i) : __ldcg(topkx + i - B * k);
+    __syncthreads();
+  }
   for (int e = w; e < E; e += warps) {
     int cnt = 0;
     for (int base = 0; base < nent; base += 32) {
       const int idx = base + lane;
-      const int ex = idx < B * k ? topk_l[idx] : idx < nent ? topkx[idx - B * k] : -1;
+      const int ex = idx >= nent ? -1 : staged ? ents[idx] : idx < B * k ? __ldcg(topk_l + idx) : __ldcg(topkx + idx - B * k);
       const bool hit = idx < nent && ex == e;
       const unsigned m = __ballot_sync(0xffffffffu, hit);
       if (hit) {
@@ -1071,15 +1161,34 @@ __global__ void k_moe_route(const float* __restrict__ rlog, int* __restrict__ to
   }
 }
 
-void launch_moe_route(const Dims& D, const Buffers& Bf, int layer, int select, const Rows& R, int32_t* dbg_topk,
-                      float* dbg_router, cudaStream_t s) {
+void launch_router_route(const Dims& D, const Buffers& Bf, const void* Wr, int layer, int select, const Rows& R,
+                         int32_t* dbg_topk, float* dbg_router, cudaStream_t s) {
   int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  const size_t rows_bytes = (size_t)2 * R.B * D.E * sizeof(float);
-  const int stage = rows_bytes <= 40 * 1024 ? 1 : 0;  // within the default dynamic shared memory
-  launch_pdl(k_moe_route, dim3(1), dim3(1024), stage ? rows_bytes : 0, s, (const float*)Bf.rlog, topk_l, Bf.topkx,
-             Bf.gate, Bf.ecount, Bf.elist, Bf.eslot, R.B, D.E, D.k, D.ka, D.maxB, select, R.has_primary(),
-             R.has_aux(), dbg_topk ? dbg_topk + (size_t)layer * R.B * D.ka : nullptr,
-             dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr, stage);
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(kRouteCl, R.B);
+  lc.blockDim = dim3(kRouteThreads);
+  lc.dynamicSmemBytes = (size_t)(2 * D.d + 2 * D.E) * sizeof(float);  // d <= 8192, E <= 1024: at most 72 KB
+  lc.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kRouteCl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  lc.attrs = at;
+  lc.numAttrs = 2;
+  int32_t* dt = dbg_topk ? dbg_topk + (size_t)layer * R.B * D.ka : nullptr;
+  float* dr = dbg_router ? dbg_router + (size_t)layer * R.B * D.E : nullptr;
+  const int prim = R.has_primary() ? 1 : 0, aux = R.has_aux() ? 1 : 0;
+  if (D.bf16)
+    cudaLaunchKernelEx(&lc, k_router_route<__nv_bfloat16>, (const __nv_bfloat16*)Wr, (const float*)Bf.un, topk_l,
+                       Bf.topkx, Bf.gate, Bf.ecount, Bf.elist, Bf.eslot, Bf.ticket, R.B, D.E, D.d, D.k, D.ka, D.maxB,
+                       select, prim, aux, dt, dr);
+  else
+    cudaLaunchKernelEx(&lc, k_router_route<float>, (const float*)Wr, (const float*)Bf.un, topk_l, Bf.topkx, Bf.gate,
+                       Bf.ecount, Bf.elist, Bf.eslot, Bf.ticket, R.B, D.E, D.d, D.k, D.ka, D.maxB, select, prim, aux,
+                       dt, dr);
 }
 
 // Expert gate/up + SwiGLU + b coupling (CUDA cores): one warp per expert
