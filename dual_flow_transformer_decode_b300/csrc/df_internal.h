@@ -142,10 +142,10 @@ void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* ou
 // Router logits rlog[m][E] of rows 0..rows-1 of an unrounded normed buffer.
 void launch_router_rows(const Dims& D, const void* Wr, const float* un, float* rlog, int rows, cudaStream_t s);
 
-// CUDA-core GEMV: out[m][n] = sum_k W[n][k] X[m][k] for rows m in [lo, hi).
-// x_f32: X is fp32 (router) instead of dtype.
-void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, int x_f32,
-                 float* out, int ldo, const Rows& R, cudaStream_t s);
+// CUDA-core GEMV: out[m][n] = sum_k W[n][k] X[m][k] for rows m in [lo, hi)
+// (W and X in the model's storage type).
+void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, float* out, int ldo,
+                 const Rows& R, cudaStream_t s);
 
 // Epilogues over the fp32 GEMM output `raw`.
 void launch_ep_qkv(const Dims& D, const Buffers& Bf, const float* raw, int ldr, const float* a,

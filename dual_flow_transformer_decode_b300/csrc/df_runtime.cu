@@ -296,7 +296,7 @@ void op_qkv(df_ctx* X, int l, const Rows& R, const Couple& C) {
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::QKV)) {
     df::tc_qkv(X->tc, D, Bf, X->wqkv[l], X->a[l], X->kv, l, C, R, X->stream);
   } else {
-    df::launch_gemv(D, X->wqkv[l], D.qkvn, D.d, Bf.u, D.d, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_gemv(D, X->wqkv[l], D.qkvn, D.d, Bf.u, D.d, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_qkv(D, Bf, Bf.raw, Bf.rawN, X->a[l], X->kv, l, C, R, X->stream);
   }
 }
@@ -319,7 +319,7 @@ void op_wo(df_ctx* X, int l, const Rows& R) {
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::RESID)) {
     df::tc_resid(X->tc, D, Bf, X->wo[l], l, R, X->stream);
   } else {
-    df::launch_gemv(D, X->wo[l], D.d, D.qdim, Bf.o, D.qdim, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_gemv(D, X->wo[l], D.d, D.qdim, Bf.o, D.qdim, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_residual(D, Bf, Bf.raw, Bf.rawN, R, X->stream);
   }
 }
@@ -331,7 +331,7 @@ void op_gateup(df_ctx* X, int l, const Rows& R, const Couple& C) {
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::SWIGLU)) {
     df::tc_swiglu(X->tc, D, Bf, X->wgu[l], l, X->b[l], C, R, X->stream);
   } else {
-    df::launch_gemv(D, X->wgu[l], 2 * D.F, D.d, Bf.u, D.d, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_gemv(D, X->wgu[l], 2 * D.F, D.d, Bf.u, D.d, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_swiglu(D, Bf, Bf.raw, Bf.rawN, X->b[l], C, R, X->stream);
   }
 }
@@ -343,7 +343,7 @@ void op_down(df_ctx* X, int l, const Rows& R, const Couple& C) {
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::DOWN)) {
     df::tc_down(X->tc, D, Bf, X->wd[l], l, X->c[l], C, R, X->stream);
   } else {
-    df::launch_gemv(D, X->wd[l], D.d, D.F, Bf.z, D.F, 0, Bf.raw, Bf.rawN, R, X->stream);
+    df::launch_gemv(D, X->wd[l], D.d, D.F, Bf.z, D.F, Bf.raw, Bf.rawN, R, X->stream);
     df::launch_ep_down(D, Bf, Bf.raw, Bf.rawN, X->c[l], C, R, X->stream);
   }
 }
@@ -370,7 +370,7 @@ void op_lm(df_ctx* X, const Rows& R) {
   if (!X->force_generic && df::tc_can_run(X->tc, df::TcOp::LOGITS)) {
     df::tc_logits(X->tc, D, Bf, X->lm_head, R, X->stream);
   } else {
-    df::launch_gemv(D, X->lm_head, D.V, D.d, Bf.u, D.d, 0, Bf.logits, D.V, R, X->stream);
+    df::launch_gemv(D, X->lm_head, D.V, D.d, Bf.u, D.d, Bf.logits, D.V, R, X->stream);
   }
 }
 

@@ -221,28 +221,70 @@ void launch_rmsnorm_rows(const Dims& D, const float* h, const float* g, void* ou
 }
 
 // ------------------------------------------------------------------ GEMV (CUDA cores)
-// One warp per output feature; lanes stride the reduction dimension with
-// coalesced loads; rows are processed R at a time with one accumulator each.
-// Each row's sum depends only on that row, so results do not change with the
-// set of active rows.
+// The CUDA-core path (fp32 models, and the forced generic sequence): one warp
+// per output feature; rows are processed R at a time with one accumulator
+// each.  With VEC16, a lane reads 16-byte chunks of the weight row and of
+// each activation row (chunk c covers elements 16c/size .. of the row, lane l
+// takes chunks l, l + 32, ...), so a warp moves 512 contiguous bytes of the
+// weight row per load; otherwise (a row length that is not a whole number of
+// chunks) elements are read one by one, lane-strided.  Each row's sum
+// depends only on that row, so results do not change with the set of active
+// rows.
 
-template <typename TW, typename TX, int R>
-__global__ void k_gemv(const TW* __restrict__ W, int N, int K, const TX* __restrict__ X, int ldx,
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& raw, float (&v)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& raw, float (&v)[4]) {
+  v[0] = __uint_as_float(raw.x);
+  v[1] = __uint_as_float(raw.y);
+  v[2] = __uint_as_float(raw.z);
+  v[3] = __uint_as_float(raw.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& raw, float (&v)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+template <typename T, int R, bool VEC16>
+__global__ void k_gemv(const T* __restrict__ W, int N, int K, const T* __restrict__ X, int ldx,
                        float* __restrict__ out, int ldo, int lo, int hi) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
+  constexpr int VEC = 16 / sizeof(T);
   int warps = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int n = blockIdx.x * warps + w; n < N; n += gridDim.x * warps) {
-    const TW* wr = W + (size_t)n * K;
+    const T* wr = W + (size_t)n * K;
     for (int r0 = lo; r0 < hi; r0 += R) {
       float acc[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = 0.f;
-      for (int k = lane; k < K; k += 32) {
-        float wv = Num<TW>::to_f(wr[k]);
+      if constexpr (VEC16) {
+        for (int k0 = lane * VEC; k0 < K; k0 += 32 * VEC) {
+          float wv[VEC];
+          unpack16<T>(*reinterpret_cast<const uint4*>(wr + k0), wv);
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (r0 + r < hi) acc[r] = fmaf(wv, Num<TX>::to_f(X[(size_t)(r0 + r) * ldx + k]), acc[r]);
+          for (int r = 0; r < R; ++r) {
+            if (r0 + r < hi) {
+              float xv[VEC];
+              unpack16<T>(*reinterpret_cast<const uint4*>(X + (size_t)(r0 + r) * ldx + k0), xv);
+#pragma unroll
+              for (int q = 0; q < VEC; ++q) acc[r] = fmaf(wv[q], xv[q], acc[r]);
+            }
+          }
+        }
+      } else {
+        for (int k = lane; k < K; k += 32) {
+          const float wv = Num<T>::to_f(wr[k]);
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if (r0 + r < hi) acc[r] = fmaf(wv, Num<T>::to_f(X[(size_t)(r0 + r) * ldx + k]), acc[r]);
+        }
       }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -253,22 +295,29 @@ __global__ void k_gemv(const TW* __restrict__ W, int N, int K, const TX* __restr
   }
 }
 
-void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, int x_f32, float* out,
-                 int ldo, const Rows& R, cudaStream_t s) {
+template <typename T>
+void launch_gemv_t(const void* W, int N, int K, const void* X, int ldx, float* out, int ldo, const Rows& R,
+                   int blocks, cudaStream_t s) {
+  constexpr int VEC = 16 / sizeof(T);
+  // 16-byte chunks need every weight and activation row to start on a chunk
+  // boundary (the buffers themselves are 256-byte aligned)
+  if (K % VEC == 0 && ldx % VEC == 0)
+    launch_pdl(k_gemv<T, 8, true>, dim3(blocks), dim3(256), 0, s, (const T*)W, N, K, (const T*)X, ldx, out, ldo,
+               R.lo, R.hi);
+  else
+    launch_pdl(k_gemv<T, 8, false>, dim3(blocks), dim3(256), 0, s, (const T*)W, N, K, (const T*)X, ldx, out, ldo,
+               R.lo, R.hi);
+}
+
+void launch_gemv(const Dims& D, const void* W, int N, int K, const void* X, int ldx, float* out, int ldo,
+                 const Rows& R, cudaStream_t s) {
   if (R.hi <= R.lo || N <= 0) return;
   int blocks = (N + 7) / 8;
   if (blocks > 148 * 16) blocks = 148 * 16;
-  if (D.bf16) {
-    if (x_f32)
-      launch_pdl(k_gemv<__nv_bfloat16, float, 8>, dim3(blocks), dim3(256), 0, s, (const __nv_bfloat16*)W, N, K, (const float*)X, ldx,
-                                                              out, ldo, R.lo, R.hi);
-    else
-      launch_pdl(k_gemv<__nv_bfloat16, __nv_bfloat16, 8>, dim3(blocks), dim3(256), 0, s, 
-          (const __nv_bfloat16*)W, N, K, (const __nv_bfloat16*)X, ldx, out, ldo, R.lo, R.hi);
-  } else {
-    launch_pdl(k_gemv<float, float, 8>, dim3(blocks), dim3(256), 0, s, (const float*)W, N, K, (const float*)X, ldx, out, ldo, R.lo,
-                                                   R.hi);
-  }
+  if (D.bf16)
+    launch_gemv_t<__nv_bfloat16>(W, N, K, X, ldx, out, ldo, R, blocks, s);
+  else
+    launch_gemv_t<float>(W, N, K, X, ldx, out, ldo, R, blocks, s);
 }
 
 // ------------------------------------------------------------------ epilogues
