@@ -348,19 +348,24 @@ void op_down(df_ctx* X, int l, const Rows& R, const Couple& C) {
   }
 }
 
-// MoE MLP with router replay (input: normed rows u and unrounded un).
-void op_moe(df_ctx* X, int l, const Rows& R, const Couple& C) {
+// MoE MLP with router replay (input: normed rows u and unrounded un).  With
+// next_norm set and the tensor-core path taken, the combine also writes the
+// RMSNorm of the updated rows with those gains into u; returns whether it
+// did.
+bool op_moe(df_ctx* X, int l, const Rows& R, const Couple& C, const float* next_norm = nullptr) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
   df::launch_router_route(D, Bf, X->router[l], l, R.has_primary() ? 1 : 0, R, X->dbg_topk, X->dbg_router, s);
   if (!X->force_generic && X->moe.enabled) {
-    df::moe_tc_forward(X->moe, D, Bf, l, X->b[l], X->c[l], C, R, s);
+    df::moe_tc_forward(X->moe, D, Bf, l, X->b[l], X->c[l], C, R, s, next_norm);
+    return next_norm != nullptr;
   } else {
     df::launch_moe_gateup_generic(D, Bf, X->wgu[l], X->b[l], C, R, s);
     df::launch_moe_down_generic(D, Bf, X->wd[l], R, s);
     df::launch_moe_combine(D, Bf, X->c[l], C, R, s);
   }
+  return false;
 }
 
 // LM head over the final-normed rows.
@@ -375,38 +380,43 @@ void op_lm(df_ctx* X, const Rows& R) {
 }
 
 // Every layer of a pass over rows R: one persistent-kernel launch where it
-// applies, else the kernel sequence per layer.
-void enqueue_layers(df_ctx* X, const Rows& R, int save, int saved) {
+// applies, else the kernel sequence per layer.  lm_norm: the final norm's
+// gains when the pass ends with the LM head (a fused MoE combine may then
+// apply it); returns whether the final norm was applied.
+bool enqueue_layers(df_ctx* X, const Rows& R, int save, int saved, const float* lm_norm = nullptr) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
   if (!X->force_generic && df::mk_can_run(X->mk, R)) {
     df::mk_launch(X->mk, D, Bf, X->kv, R, save, saved, s);
-    return;
+    return false;
   }
+  bool normed = false;  // u already holds this layer's attention-normed rows
   for (int l = 0; l < D.L; ++l) {
     Couple C = layer_couple(X, l, save, saved);
-    df::launch_rmsnorm(D, Bf, X->attn_norm[l], Bf.u, nullptr, R, s);
+    if (!normed) df::launch_rmsnorm(D, Bf, X->attn_norm[l], Bf.u, nullptr, R, s);
+    normed = false;
     op_qkv(X, l, R, C);
     op_attn(X, l, R);
     op_wo(X, l, R);
     df::launch_rmsnorm(D, Bf, X->mlp_norm[l], Bf.u, D.E ? Bf.un : nullptr, R, s);
     if (D.E) {
-      op_moe(X, l, R, C);
+      normed = op_moe(X, l, R, C, l + 1 < D.L ? X->attn_norm[l + 1] : lm_norm);
     } else {
       op_gateup(X, l, R, C);
       op_down(X, l, R, C);
     }
   }
+  return normed;
 }
 
 void enqueue_pass(df_ctx* X, const Rows& R, int save, int saved, bool lm) {
   const Dims& D = X->D;
   const Buffers& Bf = X->Bf;
   cudaStream_t s = X->stream;
-  enqueue_layers(X, R, save, saved);
+  const bool normed = enqueue_layers(X, R, save, saved, lm ? X->final_norm : nullptr);
   if (lm) {
-    df::launch_rmsnorm(D, Bf, X->final_norm, Bf.u, nullptr, R, s);
+    if (!normed) df::launch_rmsnorm(D, Bf, X->final_norm, Bf.u, nullptr, R, s);
     op_lm(X, R);
   }
 }

@@ -287,6 +287,101 @@ __global__ void k_moe_combine_tc(const float* __restrict__ yE, const float* __re
   h[(size_t)m * d + n] += y;
 }
 
+// The combine of k_moe_combine_tc followed by the RMSNorm of the updated
+// residual row with gains gn (the next layer's attention norm, or the final
+// norm), in one launch: CTA m (256 threads) takes stacked row m, thread t the
+// float4 groups t, t + 256, ... of the row, so every element's combine and
+// the row's sum of squares are computed exactly as by the two separate
+// kernels.
+__global__ void __launch_bounds__(256) k_moe_combine_norm(
+    const float* __restrict__ yE, const float* __restrict__ gate, const int* __restrict__ topk_l,
+    const int* __restrict__ topkx, const int* __restrict__ eslot, const float* __restrict__ cvec,
+    float* __restrict__ h, Couple C, int B, int lo, int d, int k, int ka, int nxe, const float* __restrict__ gn,
+    __nv_bfloat16* __restrict__ u, float eps) {
+  __shared__ size_t ofs[kCombineMaxK];
+  __shared__ float g_own[kCombineMaxK], g_prim[kCombineMaxK];
+  __shared__ float red[32];
+  const int n4 = d >> 2;
+  const float4* g4 = reinterpret_cast<const float4*>(gn);
+  float4 gv[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = threadIdx.x + q * 256;
+    if (i < n4) gv[q] = g4[i];
+  }
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  const int m = lo + blockIdx.x;
+  const int f = m >= B, b = m - f * B;
+  const int kr = f ? ka : k;
+  if (threadIdx.x < kr) {
+    const int j = threadIdx.x;
+    if (j < k) {
+      ofs[j] = ((size_t)topk_l[b * k + j] * nxe + 2 * eslot[b * k + j]) * d;
+      g_prim[j] = gate[(size_t)b * ka + j];
+    } else {
+      const int jx = j - k, ent = B * k + b * (ka - k) + jx;
+      ofs[j] = ((size_t)topkx[b * (ka - k) + jx] * nxe + 2 * eslot[ent]) * d;
+    }
+    g_own[j] = gate[(size_t)m * ka + j];
+  }
+  __syncthreads();
+  float4 v[8];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = threadIdx.x + q * 256;
+    if (i < n4) {
+      const int n = 4 * i;
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kr; ++j) {
+        const float4 e = *reinterpret_cast<const float4*>(yE + ofs[j] + (size_t)f * d + n);
+        const float gj = g_own[j];
+        y = make_float4(fmaf(gj, e.x, y.x), fmaf(gj, e.y, y.y), fmaf(gj, e.z, y.z), fmaf(gj, e.w, y.w));
+      }
+      if (f) {
+        float4 y1;
+        if (C.saved) {
+          y1 = *reinterpret_cast<const float4*>(C.y1s + (size_t)b * d + n);
+        } else {
+          y1 = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < k; ++j) {
+            const float4 e = *reinterpret_cast<const float4*>(yE + ofs[j] + n);
+            const float gj = g_prim[j];
+            y1 = make_float4(fmaf(gj, e.x, y1.x), fmaf(gj, e.y, y1.y), fmaf(gj, e.z, y1.z), fmaf(gj, e.w, y1.w));
+          }
+        }
+        const float4 c = *reinterpret_cast<const float4*>(cvec + n);
+        y = make_float4(fmaf(c.x, y1.x, y.x), fmaf(c.y, y1.y, y.y), fmaf(c.z, y1.z, y.z), fmaf(c.w, y1.w, y.w));
+      } else if (C.save) {
+        *reinterpret_cast<float4*>(C.y1s + (size_t)b * d + n) = y;
+      }
+      float4* hp = reinterpret_cast<float4*>(h + (size_t)m * d + n);
+      float4 hv = *hp;
+      hv.x += y.x;
+      hv.y += y.y;
+      hv.z += y.z;
+      hv.w += y.w;
+      *hp = hv;
+      v[q] = hv;
+      ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+    }
+  }
+  ss = block_sum(ss, red);
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = threadIdx.x + q * 256;
+    if (i < n4) {
+      const float4 gg = gv[q];
+      const float a = v[q].x * r * gg.x, bb = v[q].y * r * gg.y, c = v[q].z * r * gg.z, e = v[q].w * r * gg.w;
+      __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(u + (size_t)m * d + 4 * i);
+      o[0] = __floats2bfloat162_rn(a, bb);
+      o[1] = __floats2bfloat162_rn(c, e);
+    }
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   void* p = nullptr;
   cudaDriverEntryPointQueryResult q;
@@ -354,7 +449,7 @@ void moe_tc_free(MoePlan& P) {
 }
 
 void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int layer, const float* bvec,
-                    const float* cvec, const Couple& C, const Rows& R, cudaStream_t s) {
+                    const float* cvec, const Couple& C, const Rows& R, cudaStream_t s, const float* next_norm) {
   const int prim = R.has_primary(), aux = R.has_aux();
   launch_pdl(k_moe_gather, dim3(D.E, P.nxe), dim3(128), 0, s, (const __nv_bfloat16*)Bf.u, (const int*)Bf.ecount,
              (const int*)Bf.elist, (__nv_bfloat16*)Bf.xg, R.B, D.d, D.k, D.ka, D.maxB, P.nxe);
@@ -387,9 +482,14 @@ void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int laye
   launch_pdl(k_tc_moe, dim3(D.E * a.tiles), dim3(128), smem_bytes(P.nxe, P.stages), s, P.w_d[layer], P.x_z, D.Fe,
              a);
   const int* topk_l = Bf.topk + (size_t)layer * D.maxB * D.k;
-  launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt,
-             (const float*)Bf.gate, topk_l, (const int*)Bf.topkx, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo,
-             D.d, D.k, D.ka, P.nxe);
+  if (next_norm)
+    launch_pdl(k_moe_combine_norm, dim3(R.hi - R.lo), dim3(256), 0, s, (const float*)Bf.yEt, (const float*)Bf.gate,
+               topk_l, (const int*)Bf.topkx, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo, D.d, D.k, D.ka, P.nxe,
+               next_norm, (__nv_bfloat16*)Bf.u, D.eps);
+  else
+    launch_pdl(k_moe_combine_tc, dim3(R.hi - R.lo, (D.d + 255) / 256), dim3(256), 0, s, (const float*)Bf.yEt,
+               (const float*)Bf.gate, topk_l, (const int*)Bf.topkx, (const int*)Bf.eslot, cvec, Bf.h, C, R.B, R.lo,
+               D.d, D.k, D.ka, P.nxe);
 }
 
 }  // namespace df

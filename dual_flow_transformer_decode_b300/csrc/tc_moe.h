@@ -22,7 +22,11 @@ bool moe_tc_init(MoePlan& P, const Dims& D, const Buffers& Bf, const std::vector
                  const std::vector<const void*>& wd, std::string* err);
 void moe_tc_free(MoePlan& P);
 // Gather, gate/up + SwiGLU + b, down, combine + c + residual (routing done).
+// With next_norm set, the combine also writes the RMSNorm of the updated
+// rows with those gains into u (the next layer's attention norm, or the
+// final norm), in the same launch.
 void moe_tc_forward(const MoePlan& P, const Dims& D, const Buffers& Bf, int layer, const float* bvec,
-                    const float* cvec, const Couple& C, const Rows& R, cudaStream_t s);
+                    const float* cvec, const Couple& C, const Rows& R, cudaStream_t s,
+                    const float* next_norm = nullptr);
 
 }  // namespace df
