@@ -47,7 +47,8 @@ _lib = None
 EXPORTS = ["df_workspace_bytes", "df_create", "df_prefill", "df_set_length", "df_decode_step",
            "df_decode_step_host", "df_set_mode", "df_debug_outputs", "df_sync", "df_length",
            "df_step_kernels", "df_time_op", "df_last_error", "df_destroy", "df_decode_step_noalloc",
-           "df_generate", "df_set_batch", "df_prefill_seq", "df_release_seq", "df_seq_lengths", "df_seq_pages"]
+           "df_generate", "df_set_batch", "df_prefill_seq", "df_release_seq", "df_seq_lengths", "df_seq_pages",
+           "df_decode_step_host_async", "df_host_wait"]
 
 DF_OP = {"qkv": 0, "attn": 1, "wo": 2, "gateup": 3, "down": 4, "lmhead": 5, "moe": 6, "layers": 7}
 
@@ -86,6 +87,10 @@ def lib():
     L.df_seq_pages.restype = i
     L.df_decode_step_host.argtypes = [vp, vp, vp, vp, vp]
     L.df_decode_step_host.restype = i
+    L.df_decode_step_host_async.argtypes = [vp, vp, vp, vp, vp]
+    L.df_decode_step_host_async.restype = i
+    L.df_host_wait.argtypes = [vp]
+    L.df_host_wait.restype = i
     L.df_set_mode.argtypes = [vp, i, i]
     L.df_set_mode.restype = i
     L.df_debug_outputs.argtypes = [vp, vp, vp, vp, vp]
@@ -176,6 +181,17 @@ def df_set_mode(ctx, aux_on: int, ungrouped: int) -> None:
 def df_debug_outputs(ctx, logp1: int = 0, logp2: int = 0, topk: int = 0, router: int = 0) -> None:
     check(ctx, lib().df_debug_outputs(ctx, C.c_void_p(logp1 or None), C.c_void_p(logp2 or None),
                                       C.c_void_p(topk or None), C.c_void_p(router or None)), "df_debug_outputs")
+
+
+def df_decode_step_host_async(ctx, tokens_ptr: int, logp_mix_ptr: int = 0, argmax_ptr: int = 0,
+                              alpha_ptr: int = 0) -> None:
+    check(ctx, lib().df_decode_step_host_async(ctx, C.c_void_p(tokens_ptr), C.c_void_p(logp_mix_ptr or None),
+                                               C.c_void_p(argmax_ptr or None), C.c_void_p(alpha_ptr or None)),
+          "df_decode_step_host_async")
+
+
+def df_host_wait(ctx) -> None:
+    check(ctx, lib().df_host_wait(ctx), "df_host_wait")
 
 
 def df_sync(ctx) -> None:

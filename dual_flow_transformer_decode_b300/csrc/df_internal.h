@@ -89,6 +89,9 @@ struct Buffers {
   float* out_logp;  // [maxB][V] host-step staging
   int* out_arg;     // [maxB]
   float* out_alpha; // [maxB]
+  float* out_logp2; // second staging area of the pipelined host step
+  int* out_arg2;
+  float* out_alpha2;
   int* gen_tok;     // [maxB] generation: the next step's input tokens (written by the draw)
   int* gen_hist;    // [max_len][maxB] generation: the token drawn at each position
   float* rope;      // [max_len][hd/2][2] cos, sin

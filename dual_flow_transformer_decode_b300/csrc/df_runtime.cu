@@ -86,6 +86,12 @@ struct df_ctx {
   GraphSlot dec, pre;
   GraphSlot dec_static;  // graph of df_decode_step_noalloc
   GraphSlot gen;         // graph of one df_generate step
+  // pipelined host-buffer steps: output copies on their own stream, from two
+  // staging areas used in turn (each with its own captured step graph)
+  GraphSlot dec_host[2];
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t step_done[2] = {nullptr, nullptr}, copy_done[2] = {nullptr, nullptr};
+  int host_slot = 0;
   int last_kernels = -1;
   df::TcPlan tc;
   df::MoePlan moe;
@@ -258,6 +264,9 @@ size_t layout(const Dims& D, Buffers* Bf, char* base) {
   b.out_logp = (float*)take((size_t)D.maxB * D.V * 4);
   b.out_arg = (int*)take(D.maxB * 4);
   b.out_alpha = (float*)take(D.maxB * 4);
+  b.out_logp2 = (float*)take((size_t)D.maxB * D.V * 4);
+  b.out_arg2 = (int*)take(D.maxB * 4);
+  b.out_alpha2 = (float*)take(D.maxB * 4);
   b.gen_tok = (int*)take(D.maxB * 4);
   b.gen_hist = (int*)take((size_t)D.max_len * D.maxB * 4);
   b.rope = (float*)take((size_t)(D.max_len + 1) * D.hd * 4);
@@ -749,6 +758,8 @@ static df_status set_batch(df_ctx* X, int B) {
   }
   if (B != X->B) {
     X->dec.reset();
+    X->dec_host[0].reset();
+    X->dec_host[1].reset();
     X->pre.reset();
     X->dec_static.reset();
     X->gen.reset();
@@ -835,10 +846,9 @@ df_status df_set_length(df_ctx* X, int B, int t) {
   return e == cudaSuccess ? DF_OK : cuda_fail(X, e, "df_set_length");
 }
 
-df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax, float* alpha) {
-  if (!X) return DF_ERR_ARG;
-  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step: null tokens");
-  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step before df_prefill");
+// One decode step replayed from the graph cached in `slot`.
+static df_status decode_into(df_ctx* X, GraphSlot& slot, const int32_t* tokens, float* logp_mix, int32_t* argmax,
+                             float* alpha) {
   df_status pst = prepare_steps(X, 1, "df_decode_step");
   if (pst != DF_OK) return pst;
   GraphKey key{};
@@ -855,10 +865,17 @@ df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int3
   key.i[2] = X->B;
   key.i[3] = X->force_generic;
   StepOut o{logp_mix, argmax, alpha};
-  df_status st = run_captured(X, X->dec, key, [&] { enqueue_decode(X, tokens, o); }, 1);
+  df_status st = run_captured(X, slot, key, [&] { enqueue_decode(X, tokens, o); }, 1);
   if (st != DF_OK) return st;
   finish_steps(X, 1);
   return DF_OK;
+}
+
+df_status df_decode_step(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax, float* alpha) {
+  if (!X) return DF_ERR_ARG;
+  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step: null tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step before df_prefill");
+  return decode_into(X, X->dec, tokens, logp_mix, argmax, alpha);
 }
 
 df_status df_generate(df_ctx* X, const int32_t* tokens, int n_steps, unsigned long long seed, int32_t* out_tokens,
@@ -927,7 +944,11 @@ df_status df_decode_step_host(df_ctx* X, const int32_t* tokens, float* logp_mix,
   df_status pst = prepare_steps(X, 1, "df_decode_step_host");  // capacity before any copy
   if (pst != DF_OK) return pst;
   int B = X->B, V = X->D.V;
-  cudaError_t e = cudaMemcpyAsync(X->Bf.tokbuf, tokens, B * sizeof(int32_t), cudaMemcpyHostToDevice, X->stream);
+  cudaError_t e = cudaSuccess;
+  // staging area 0 may still be copied out by a pipelined step
+  if (X->copy_done[0]) e = cudaStreamWaitEvent(X->stream, X->copy_done[0], 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(X->Bf.tokbuf, tokens, B * sizeof(int32_t), cudaMemcpyHostToDevice, X->stream);
   if (e != cudaSuccess) return cuda_fail(X, e, "token copy");
   df_status st = df_decode_step(X, X->Bf.tokbuf, logp_mix ? X->Bf.out_logp : nullptr, argmax ? X->Bf.out_arg : nullptr,
                                 alpha ? X->Bf.out_alpha : nullptr);
@@ -936,6 +957,57 @@ df_status df_decode_step_host(df_ctx* X, const int32_t* tokens, float* logp_mix,
   if (e == cudaSuccess && argmax) e = cudaMemcpyAsync(argmax, X->Bf.out_arg, B * 4, cudaMemcpyDeviceToHost, X->stream);
   if (e == cudaSuccess && alpha) e = cudaMemcpyAsync(alpha, X->Bf.out_alpha, B * 4, cudaMemcpyDeviceToHost, X->stream);
   if (e != cudaSuccess) return cuda_fail(X, e, "output copy");
+  return df_sync(X);
+}
+
+df_status df_decode_step_host_async(df_ctx* X, const int32_t* tokens, float* logp_mix, int32_t* argmax,
+                                    float* alpha) {
+  if (!X) return DF_ERR_ARG;
+  if (!tokens) return fail(X, DF_ERR_ARG, "df_decode_step_host_async: null tokens");
+  if (!X->ready) return fail(X, DF_ERR_STATE, "df_decode_step_host_async before df_prefill");
+  df_status pst = prepare_steps(X, 1, "df_decode_step_host_async");  // capacity before any copy
+  if (pst != DF_OK) return pst;
+  cudaError_t e = cudaSuccess;
+  if (!X->copy_stream) {
+    e = cudaStreamCreateWithFlags(&X->copy_stream, cudaStreamNonBlocking);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&X->step_done[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&X->copy_done[k], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(X, e, "df_decode_step_host_async: copy stream");
+  }
+  const int k = X->host_slot;
+  const int B = X->B, V = X->D.V;
+  float* dl = k ? X->Bf.out_logp2 : X->Bf.out_logp;
+  int32_t* da = k ? X->Bf.out_arg2 : X->Bf.out_arg;
+  float* dp = k ? X->Bf.out_alpha2 : X->Bf.out_alpha;
+  // this staging area's previous contents must have left before the step
+  // writes it again
+  e = cudaStreamWaitEvent(X->stream, X->copy_done[k], 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(X->Bf.tokbuf, tokens, B * sizeof(int32_t), cudaMemcpyHostToDevice, X->stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_decode_step_host_async: token copy");
+  df_status st = decode_into(X, X->dec_host[k], X->Bf.tokbuf, logp_mix ? dl : nullptr, argmax ? da : nullptr,
+                             alpha ? dp : nullptr);
+  if (st != DF_OK) return st;
+  e = cudaEventRecord(X->step_done[k], X->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(X->copy_stream, X->step_done[k], 0);
+  if (e == cudaSuccess && logp_mix)
+    e = cudaMemcpyAsync(logp_mix, dl, (size_t)B * V * 4, cudaMemcpyDeviceToHost, X->copy_stream);
+  if (e == cudaSuccess && argmax) e = cudaMemcpyAsync(argmax, da, B * 4, cudaMemcpyDeviceToHost, X->copy_stream);
+  if (e == cudaSuccess && alpha) e = cudaMemcpyAsync(alpha, dp, B * 4, cudaMemcpyDeviceToHost, X->copy_stream);
+  if (e == cudaSuccess) e = cudaEventRecord(X->copy_done[k], X->copy_stream);
+  if (e != cudaSuccess) return cuda_fail(X, e, "df_decode_step_host_async: output copy");
+  X->host_slot = k ^ 1;
+  return DF_OK;
+}
+
+df_status df_host_wait(df_ctx* X) {
+  if (!X) return DF_ERR_ARG;
+  if (X->copy_stream) {
+    cudaError_t e = cudaStreamSynchronize(X->copy_stream);
+    if (e != cudaSuccess) return cuda_fail(X, e, "df_host_wait");
+  }
   return df_sync(X);
 }
 
@@ -1082,6 +1154,15 @@ const char* df_last_error(const df_ctx* X) { return X ? X->err.c_str() : "null c
 void df_destroy(df_ctx* X) {
   if (!X) return;
   if (X->stream) cudaStreamSynchronize(X->stream);
+  if (X->copy_stream) {
+    cudaStreamSynchronize(X->copy_stream);
+    cudaStreamDestroy(X->copy_stream);
+  }
+  for (int k = 0; k < 2; ++k) {
+    if (X->step_done[k]) cudaEventDestroy(X->step_done[k]);
+    if (X->copy_done[k]) cudaEventDestroy(X->copy_done[k]);
+    X->dec_host[k].reset();
+  }
   X->dec.reset();
   X->pre.reset();
   X->dec_static.reset();

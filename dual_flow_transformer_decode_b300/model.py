@@ -151,6 +151,19 @@ class DualFlowModel:
                                argmax.data_ptr() if argmax is not None else 0,
                                alpha.data_ptr() if alpha is not None else 0)
 
+    def decode_step_host_async(self, tokens: torch.Tensor, logp_mix: torch.Tensor | None = None,
+                               argmax: torch.Tensor | None = None, alpha: torch.Tensor | None = None) -> None:
+        """Pipelined host-buffer step: returns at once; the outputs are valid,
+        and the buffers free, after host_wait()."""
+        assert tokens.dtype == torch.int32 and not tokens.is_cuda
+        _b.df_decode_step_host_async(self.ctx, tokens.data_ptr(),
+                                     logp_mix.data_ptr() if logp_mix is not None else 0,
+                                     argmax.data_ptr() if argmax is not None else 0,
+                                     alpha.data_ptr() if alpha is not None else 0)
+
+    def host_wait(self) -> None:
+        _b.df_host_wait(self.ctx)
+
     def set_mode(self, aux_on: bool = True, ungrouped: bool = False) -> None:
         _b.df_set_mode(self.ctx, int(aux_on), int(ungrouped))
 

@@ -161,6 +161,23 @@ df_status df_decode_step(df_ctx* ctx, const int32_t* tokens, float* logp_mix, in
 df_status df_decode_step_host(df_ctx* ctx, const int32_t* tokens, float* logp_mix,
                               int32_t* argmax, float* alpha);
 
+/* Pipelined form of df_decode_step_host for callers whose next tokens do not
+ * depend on this step's outputs (teacher forcing, scoring): enqueues the
+ * copy of tokens (host int32 [B]) to the device, the step, and the copies of
+ * the outputs (host, each may be NULL) back to the host, and returns without
+ * waiting.  The output copies run on a second stream of the context from one
+ * of two device staging areas used in turn, so they overlap the next step's
+ * kernels.  The host buffers belong to the library until df_host_wait
+ * returns: tokens must not change and the outputs are not valid before
+ * then.  Errors of the enqueue are returned at once; device-detected errors
+ * by df_host_wait. */
+df_status df_decode_step_host_async(df_ctx* ctx, const int32_t* tokens, float* logp_mix,
+                                    int32_t* argmax, float* alpha);
+
+/* Waits until every step enqueued by df_decode_step_host_async has
+ * completed and its outputs are in host memory, then reports like df_sync. */
+df_status df_host_wait(df_ctx* ctx);
+
 /* Generation: n_steps decode steps on the device, each fed the token drawn
  * from p_mix at the step before ("Problema Central": decode generates tokens
  * one at a time; "Mecanismos Clave", Objetivo de Mezcla: p_mix is the

@@ -89,3 +89,35 @@ def test_host_buffer_step_matches_device_step(cuda_device):
         np.testing.assert_array_equal(al.double().numpy(), ref.steps[s]["alpha"])
     m.close()
     ref.close()
+
+
+@pytest.mark.parametrize("name", ["t_bf16", "t_moe"])
+def test_pipelined_host_steps_match_device_steps(name, cuda_device):
+    """df_decode_step_host_async: every step's outputs, copied out on the
+    second stream from alternating staging areas, equal the device-buffer
+    steps bit for bit; a synchronous host step in between waits for the
+    pipelined copies of its staging area."""
+    import torch
+    from dual_flow_transformer_decode_b300.model import DualFlowModel
+    cfg = dfsynth.get_config(name).with_(n_steps=5)
+    w = Weights(cfg, 0)
+    tok = dfsynth.tokens(cfg, 0)
+    ref = GpuRun(cfg, w, tok)
+    m = DualFlowModel(cfg, w)
+    m.prefill(torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda())
+    B, V, n = cfg.batch, cfg.vocab, cfg.n_steps
+    lp = [torch.full((B, V), float("nan")).pin_memory() for _ in range(n)]
+    am = [torch.full((B,), -1, dtype=torch.int32).pin_memory() for _ in range(n)]
+    al = [torch.full((B,), float("nan")).pin_memory() for _ in range(n)]
+    toks = [torch.from_numpy(tok[:, cfg.n_prefill + s].copy()).pin_memory() for s in range(n)]
+    for s in range(3):
+        m.decode_step_host_async(toks[s], lp[s], am[s], al[s])
+    m.decode_step_host(toks[3], lp[3], am[3], al[3])
+    m.decode_step_host_async(toks[4], lp[4], am[4], al[4])
+    m.host_wait()
+    for s in range(n):
+        np.testing.assert_array_equal(lp[s].double().numpy(), ref.steps[s]["logp_mix"])
+        np.testing.assert_array_equal(am[s].numpy(), ref.steps[s]["argmax"])
+        np.testing.assert_array_equal(al[s].double().numpy(), ref.steps[s]["alpha"])
+    m.close()
+    ref.close()
