@@ -91,19 +91,22 @@ def test_host_buffer_step_matches_device_step(cuda_device):
     ref.close()
 
 
-@pytest.mark.parametrize("name", ["t_bf16", "t_moe"])
-def test_pipelined_host_steps_match_device_steps(name, cuda_device):
+@pytest.mark.parametrize("name,aux,ungrouped", [("t_bf16", True, False), ("t_moe", True, False),
+                                               ("t_bf16", False, False), ("t_moe", True, True)])
+def test_pipelined_host_steps_match_device_steps(name, aux, ungrouped, cuda_device):
     """df_decode_step_host_async: every step's outputs, copied out on the
     second stream from alternating staging areas, equal the device-buffer
-    steps bit for bit; a synchronous host step in between waits for the
-    pipelined copies of its staging area."""
+    steps bit for bit (grouped, auxiliary flow off, ungrouped two-pass); a
+    synchronous host step in between waits for the pipelined copies of its
+    staging area."""
     import torch
     from dual_flow_transformer_decode_b300.model import DualFlowModel
     cfg = dfsynth.get_config(name).with_(n_steps=5)
     w = Weights(cfg, 0)
     tok = dfsynth.tokens(cfg, 0)
-    ref = GpuRun(cfg, w, tok)
+    ref = GpuRun(cfg, w, tok, aux=aux, ungrouped=ungrouped)
     m = DualFlowModel(cfg, w)
+    m.set_mode(aux, ungrouped)
     m.prefill(torch.from_numpy(tok[:, :cfg.n_prefill].copy()).cuda())
     B, V, n = cfg.batch, cfg.vocab, cfg.n_steps
     lp = [torch.full((B, V), float("nan")).pin_memory() for _ in range(n)]
